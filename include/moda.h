@@ -1,0 +1,116 @@
+/*
+ * moda.h -- C ABI of the Mixture-of-Depths Attention (MoDA) forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * MoDA (arXiv 2603.15619, Sec. 2.2 "Mixture-of-Depths Attention", Fig. 1):
+ * every grouped-query attention head at token t attends, under ONE softmax,
+ * to the causal sequence keys/values of its own layer (positions <= t) and to
+ * the L depth key/value slots that earlier layers (attention layers and the
+ * FFN-input KV projections) wrote for the SAME position t.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE memory owned by the caller, dense,
+ *     row-major, bf16 unless stated, 16-byte aligned. The library never
+ *     allocates memory per call and never frees caller memory.
+ *   - Calls enqueue work on `stream` (0 = the legacy default stream) and
+ *     return after the launch; results are ready when the stream is.
+ *   - Argument errors are reported synchronously by the return value and
+ *     nothing is launched. A failure inside a running kernel (a bounded wait
+ *     that gave up) is latched in a per-device error word and reported by
+ *     moda_get_device_error().
+ *   - Batch is 1; callers loop over sequences.
+ *   - Thread safety: calls may be made from several host threads; the
+ *     tensor-map cache is guarded by a mutex.
+ */
+#ifndef MODA_H_
+#define MODA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moda_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MODA_OK = 0,
+  MODA_ERR_INVALID_ARG = 1, /* NULL pointer, T < 1, L < 0, Hq % Hk != 0, aliasing */
+  MODA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}; G = Hq/Hk not in {1,2,4,8,16}; sizes too large */
+  MODA_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned */
+  MODA_ERR_CUDA = 4,        /* the CUDA runtime reported an error at launch */
+  MODA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (device-side) */
+  MODA_ERR_NO_DEVICE = 6    /* no CUDA device of compute capability 10.3 is current */
+} moda_status;
+
+/*
+ * moda_pack_depth -- relayout the depth stream into the flash-compatible,
+ * chunk-aware order (Sec. 3.2 "Flash-compatible depth KV layout" and
+ * "Chunk-aware depth KV layout", Fig. 4): the L slots of each position become
+ * contiguous, so a query tile covering positions [t0, t1) of KV head hk reads
+ * one contiguous block dst[hk][t0..t1)[0..L)[:].
+ *
+ *   dst[hk][t][l][c] = src[l][t][hk][c]      (bit-exact copy)
+ *
+ *   src  [L, T, Hk, d] bf16 -- slot l is what the l-th earlier layer appended
+ *   dst  [Hk, T, L, d] bf16 -- must not overlap src
+ *   d    64 or 128
+ * Call once for the depth keys and once for the depth values. L == 0 is a
+ * no-op (src and dst may then be NULL).
+ * Errors: INVALID_ARG (NULL with L > 0, T < 1, Hk < 1, L < 0, src == dst),
+ * UNSUPPORTED (d), MISALIGNED, CUDA.
+ */
+moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk,
+                            int d, moda_stream_t stream);
+
+/*
+ * moda_fwd -- the MoDA forward (Sec. 2.2 joint softmax; Sec. 3.3 fused
+ * kernel: group-aware query tiles, grouped causal mask, block-diagonal depth
+ * mask, one online-softmax state).
+ *
+ * For every position t < T and query head h < Hq, with G = Hq / Hk and
+ * hk = floor(h / G) (contiguous groups of G query heads share KV head hk,
+ * Sec. 2.1 Eq. (2) phi(h) read 0-based):
+ *   z = [ scale * q[t,h,:].k[j,hk,:]   for j = 0..t          (causal, self included)
+ *       | scale * q[t,h,:].kd[hk,t,l,:] for l = 0..L-1 ]      (depth slots of position t)
+ *   o[t,h,:] = sum softmax(z) * [ v[j,hk,:] | vd[hk,t,l,:] ]   (one shared denominator)
+ *   lse[t,h] = ln(sum exp(z))   (natural log, scaled-score domain)
+ *
+ *   q       [T, Hq, d] bf16
+ *   k, v    [T, Hk, d] bf16
+ *   kd, vd  [Hk, T, L, d] bf16, the PACKED depth stream (moda_pack_depth);
+ *           may be NULL when L == 0, which makes the call plain causal GQA
+ *   scale   the logit scale, usually 1/sqrt(d); used for sequence and depth
+ *   o       [T, Hq, d] bf16 output, rounded to nearest even
+ *   lse     [T, Hq] fp32 output (may be NULL if not wanted)
+ * Arithmetic: bf16 products, fp32 accumulation, softmax in fp32 through exp2
+ * with log2(e) folded into the scale, probabilities rounded to bf16 before
+ * the P.V product.
+ * Outputs must not overlap inputs. Supported: d in {64, 128},
+ * G in {1, 2, 4, 8, 16}, 1 <= T <= 2^24, 0 <= L <= 1024.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA (synchronous);
+ * TIMEOUT via moda_get_device_error.
+ */
+moda_status moda_fwd(const void* q, const void* k, const void* v,
+                     const void* kd, const void* vd, int T, int Hq, int Hk,
+                     int d, int L, float scale, void* o, float* lse,
+                     moda_stream_t stream);
+
+/*
+ * moda_get_device_error -- synchronises `stream`, then returns and clears
+ * the current device's latched kernel error word (MODA_OK if none).
+ */
+moda_status moda_get_device_error(moda_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* moda_status_string(moda_status s);
+
+/* Detail of the last non-OK status returned on the calling host thread
+ * (which argument, which CUDA error). Never NULL. */
+const char* moda_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MODA_H_ */

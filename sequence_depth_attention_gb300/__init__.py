@@ -1,0 +1,12 @@
+"""MoDA (Mixture-of-Depths Attention) forward on GB300 (sm_103a).
+
+Thin Python face of the C-ABI library ``libmoda.so`` (declared in
+``include/moda.h``): argument marshalling only, every step of the path runs in
+the library's CUDA kernels. The library is loaded on first use and its absence
+is an error; there is no CPU fallback.
+"""
+from .binding import (MODA_OK, ModaError, moda_fwd, moda_get_device_error,
+                      moda_pack_depth, moda_status_string, library_path, load)
+
+__all__ = ["MODA_OK", "ModaError", "moda_fwd", "moda_get_device_error",
+           "moda_pack_depth", "moda_status_string", "library_path", "load"]

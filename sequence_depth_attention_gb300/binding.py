@@ -1,0 +1,149 @@
+"""ctypes binding of ``libmoda.so``: the calls of ``include/moda.h`` with the
+same names, taking torch CUDA tensors and marshalling their pointers and the
+current stream. Every step of the computation runs in the library's kernels;
+this module only allocates outputs when the caller does not pass them.
+
+The library is built in-tree (``python -m sequence_depth_attention_gb300.build``
+or ``__graft_entry__.build()``) into ``sequence_depth_attention_gb300/_build``.
+If it is missing, loading raises ``ModaError``: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(_HERE, "_build", "libmoda.so")
+
+MODA_OK = 0
+_STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
+           3: "MODA_ERR_MISALIGNED", 4: "MODA_ERR_CUDA", 5: "MODA_ERR_TIMEOUT",
+           6: "MODA_ERR_NO_DEVICE"}
+
+# every symbol include/moda.h declares
+EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_get_device_error",
+           "moda_status_string", "moda_last_error_detail")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ModaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = _STATUS.get(status, f"status {status}")
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def load():
+    """Load libmoda.so once; raises ModaError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB):
+            raise ModaError(6, "load", f"{_LIB} is missing; build it with "
+                            "`python -m sequence_depth_attention_gb300.build`")
+        lib = ctypes.CDLL(_LIB)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.moda_pack_depth.argtypes = [vp, vp, i, i, i, i, vp]
+        lib.moda_pack_depth.restype = i
+        lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
+        lib.moda_fwd.restype = i
+        lib.moda_get_device_error.argtypes = [vp]
+        lib.moda_get_device_error.restype = i
+        lib.moda_status_string.argtypes = [i]
+        lib.moda_status_string.restype = ctypes.c_char_p
+        lib.moda_last_error_detail.argtypes = []
+        lib.moda_last_error_detail.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def moda_status_string(status: int) -> str:
+    return load().moda_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != MODA_OK:
+        detail = load().moda_last_error_detail().decode()
+        raise ModaError(status, where, detail)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def moda_pack_depth(src: torch.Tensor, dst: torch.Tensor | None = None, stream=None):
+    """[L,T,Hk,d] -> [Hk,T,L,d] (bit-exact). Returns dst."""
+    _need(src, "src")
+    L, T, Hk, d = src.shape
+    if dst is None:
+        dst = torch.empty((Hk, T, L, d), dtype=src.dtype, device=src.device)
+    _need(dst, "dst")
+    if tuple(dst.shape) != (Hk, T, L, d):
+        raise ValueError(f"dst: expected shape {(Hk, T, L, d)}, got {tuple(dst.shape)}")
+    st = load().moda_pack_depth(_ptr(src), _ptr(dst), L, T, Hk, d, _stream(stream))
+    _check(st, "moda_pack_depth")
+    return dst
+
+
+def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
+             want_lse: bool = True):
+    """MoDA forward. q[T,Hq,d], k/v[T,Hk,d], kd/vd packed [Hk,T,L,d] (or
+    None when L == 0). Returns (o[T,Hq,d] bf16, lse[T,Hq] fp32 or None)."""
+    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    T, Hq, d = q.shape
+    Hk = k.shape[1]
+    if tuple(k.shape) != (T, Hk, d) or tuple(v.shape) != (T, Hk, d):
+        raise ValueError("k and v must be [T,Hk,d] matching q[T,Hq,d]")
+    if kd is None or kd.numel() == 0:
+        L = 0 if kd is None else kd.shape[2]
+        if L != 0:
+            raise ValueError("empty kd with L > 0")
+        kd = vd = None
+    else:
+        _need(kd, "kd"), _need(vd, "vd")
+        L = kd.shape[2]
+        if tuple(kd.shape) != (Hk, T, L, d) or tuple(vd.shape) != (Hk, T, L, d):
+            raise ValueError(f"kd/vd must be packed [Hk,T,L,d] = {(Hk, T, L, d)}")
+    if o is None:
+        o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=q.device)
+    _need(o, "o")
+    if want_lse and lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    st = load().moda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L,
+                         float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check(st, "moda_fwd")
+    return o, lse
+
+
+def moda_get_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device's kernel error word."""
+    return int(load().moda_get_device_error(_stream(stream)))
