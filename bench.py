@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark of the MoDA forward hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...        # the fp64 CPU oracle arm
+
+One step = the whole hot path over one batch of synthetic input resident in
+HBM: moda_pack_depth(kd), moda_pack_depth(vd), moda_fwd(...). The headline
+workload is the long-context layer (T=65536, Hq=16, Hk=4, d=128, L=48).
+Throughput counts 4*d*Hq*(T(T+1)/2 + T*L) FLOPs per step (causal and valid
+depth work only). Under torchrun each rank runs an independent replica on its
+own GPU (weak scaling); value = all ranks' FLOPs / the slowest rank's time.
+
+Also reported on the same JSON line:
+  fwd             moda_fwd alone (CUDA events on its stream), % of bf16 peak
+  overhead_vs_L0  t_fwd(L) / t_fwd(L=0) - 1 for the same T, Hq, Hk, d
+  roofline        the dominant kernel (moda_fwd) against the measured peak
+  e2e             same metric with inputs copied from pinned host memory and
+                  o, lse copied back inside the timed region
+  cpu_baseline    the fp64 oracle on the host cores, on a bounded row sample
+  clocks          nvidia-smi samples taken during the timed region
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sequence_depth_attention_gb300 import inputs as wl  # noqa: E402
+
+METRIC = "MoDA fwd TFLOP/s and % bf16 tensor peak at T=64K; overhead vs L=0"
+FWD_SOURCES = ["sequence_depth_attention_gb300/csrc/fwd_mma.cu"]
+PACK_SOURCES = ["sequence_depth_attention_gb300/csrc/pack_depth.cu"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_by_name(name):
+    for w in [*wl.ALL, wl.LONG_L0]:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}; known: {[w.name for w in wl.ALL]}")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, paths):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != sources_sha(paths):
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi -lms 200 while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        ident = None
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            ident = u if u.startswith("GPU-") else f"GPU-{u}"
+        except Exception:
+            ident = None
+        self.ident = ident
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.ident:
+            cmd += ["-i", self.ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU arm
+def oracle_sample(w, host, rows_budget_s, seed=0, nthreads=None):
+    """Time the fp64 oracle on a seeded sample of rows for about rows_budget_s
+    seconds. Returns (flops, seconds, rows, threads)."""
+    import numpy as np
+
+    import oracle
+    from sequence_depth_attention_gb300.inputs import bf16_bits
+    nthreads = nthreads or (os.cpu_count() or 1)
+    b = {n: bf16_bits(t) for n, t in host.items()}
+    kd = b["kd"] if w.L else None
+    vd = b["vd"] if w.L else None
+    rng = np.random.default_rng(seed)
+    flops = 0.0
+    rows = 0
+    t0 = time.perf_counter()
+    batch = nthreads
+    while True:
+        ts = rng.integers(0, w.T, size=batch)
+        hs = rng.integers(0, w.Hq, size=batch)
+        oracle.rows(b["q"], b["k"], b["v"], kd, vd, w.scale, ts, hs, nthreads=nthreads)
+        flops += float(np.sum(4.0 * w.d * (ts + 1 + w.L)))
+        rows += batch
+        el = time.perf_counter() - t0
+        if el >= rows_budget_s:
+            return flops, el, rows, nthreads
+        batch = min(batch * 2, max(nthreads, int(rows * (rows_budget_s - el) / max(el, 1e-3))))
+
+
+def host_inputs(w):
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = wl.make_inputs(w, device=dev)
+    return {n: t.cpu() for n, t in x.items()}
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    host = host_inputs(w)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_sample(w, host, per_step, seed=1000 + i)
+    flops = secs = 0.0
+    rows = threads = 0
+    for i in range(args.steps):
+        f, s, r, threads = oracle_sample(w, host, per_step, seed=i)
+        flops += f
+        secs += s
+        rows += r
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} (t, h) rows drawn uniformly from the {w.name} workload "
+                                   f"(seeded), ~{per_step:.0f} s of oracle work per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, n):
+    kvd = 2 * w.L * w.T * w.Hk * w.d * 2
+    return {"workload": w.name, "T": w.T, "Hq": w.Hq, "Hk": w.Hk, "G": w.G, "d": w.d, "L": w.L,
+            "batch": 1, "causal": True, "scale": "1/sqrt(d)",
+            "step": "moda_pack_depth(kd) + moda_pack_depth(vd) + moda_fwd",
+            "l2": f"inputs larger than L2 (kd+vd {kvd / 1e9:.2f} GB, q {w.T * w.Hq * w.d * 2 / 1e6:.0f} MB)",
+            "parallelism": f"replicas x{n}" if n > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="moda", choices=["moda", "reference"])
+    ap.add_argument("--workload", default=wl.LONG.name)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "moda":
+        print("note: warm-up raised to the minimum of 3", file=sys.stderr)
+        args.warmup = 3
+    w = workload_by_name(args.workload)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank)
+
+    import sequence_depth_attention_gb300 as moda
+    from sequence_depth_attention_gb300 import build as mbuild
+    mbuild.build()
+    moda.load()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    x = wl.make_inputs(w, device=dev)
+    q, k, v, kd_raw, vd_raw = (x[n] for n in ("q", "k", "v", "kd", "vd"))
+    kd = torch.empty((w.Hk, w.T, w.L, w.d), dtype=torch.bfloat16, device=dev)
+    vd = torch.empty_like(kd)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device=dev)
+    K, W = args.steps, args.warmup
+    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    pack_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+
+    def step(i=None):
+        if i is not None:
+            pack_ev[i][0].record(stream)
+        if w.L:
+            moda.moda_pack_depth(kd_raw, kd, stream=stream)
+            moda.moda_pack_depth(vd_raw, vd, stream=stream)
+        if i is not None:
+            pack_ev[i][1].record(stream)
+            fwd_ev[i][0].record(stream)
+        moda.moda_fwd(q, k, v, kd if w.L else None, vd if w.L else None, w.scale, o=o, lse=lse,
+                      stream=stream)
+        if i is not None:
+            fwd_ev[i][1].record(stream)
+
+    launches_per_step = (2 if w.L else 0) + 1
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(val):
+        if dist is None:
+            return val
+        t = torch.tensor([val], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(W):
+        step()
+    st = moda.moda_get_device_error(stream)
+    if st != 0:
+        raise SystemExit(f"device error after warm-up: {moda.moda_status_string(st)}")
+
+    clocks = ClockSampler(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(K):
+        step(i)
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_step = max_over_ranks(start.elapsed_time(end) / K)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    pack_ms = statistics.mean(a.elapsed_time(b) for a, b in pack_ev)
+    st = moda.moda_get_device_error(stream)
+    if st != 0:
+        raise SystemExit(f"device error in timed region: {moda.moda_status_string(st)}")
+
+    # plain causal GQA (L = 0) with the same kernel, same T/Hq/Hk/d
+    w0 = w.with_L(0)
+    for _ in range(W):
+        moda.moda_fwd(q, k, v, None, None, w.scale, o=o, lse=lse, stream=stream)
+    e0 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for a, b in e0:
+        a.record(stream)
+        moda.moda_fwd(q, k, v, None, None, w.scale, o=o, lse=lse, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd0_ms = statistics.mean(a.elapsed_time(b) for a, b in e0)
+
+    peaks, peaks_src = load_peaks()
+    F = w.flops()
+    value = world * F / (ms_step * 1e-3) / 1e12
+    fwd_tflops = F / (fwd_ms * 1e-3) / 1e12
+    fwd0_tflops = w0.flops() / (fwd0_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    pack_bytes = 2 * 2 * (w.L * w.T * w.Hk * w.d * 2)  # read + write, kd and vd
+    traffic = recorded_traffic("moda_fwd", w.name, FWD_SOURCES)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, world),
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tflops, "pct_peak_burst": 100 * fwd_tflops / peak,
+                "pct_peak_sustained": 100 * fwd_tflops / peak_sus,
+                "flops_per_launch": F},
+        "fwd_L0": {"ms": fwd0_ms, "tflops": fwd0_tflops, "pct_peak_burst": 100 * fwd0_tflops / peak},
+        "overhead_vs_L0": fwd_ms / fwd0_ms - 1.0,
+        "extra_time_pages_convention": 1.0 - fwd0_ms / fwd_ms,
+        "pack": {"ms_for_kd_and_vd": pack_ms,
+                 "gbs": (pack_bytes / (pack_ms * 1e-3) / 1e9) if w.L and pack_ms > 0 else None,
+                 "pct_hbm": (100 * pack_bytes / (pack_ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
+                 if w.L and pack_ms > 0 else None},
+        "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": fwd_tflops / peak, "traffic": traffic,
+                     "peak_source": f"{peaks_src} bf16 dense burst (MEASURED_PEAKS.json)"
+                     if peaks_src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "moda_fwd"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+
+    # ---- end to end: pinned host inputs in, o and lse out, every step ----
+    if not args.no_e2e:
+        hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hkd, hvd = (t.cpu().pin_memory() for t in (kd_raw, vd_raw))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            if w.L:
+                kd_raw.copy_(hkd, non_blocking=True)
+                vd_raw.copy_(hvd, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(W):
+            e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / K)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv)) + \
+            (sum(t.numel() * t.element_size() for t in (hkd, hvd)) if w.L else 0)
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        line["e2e"] = {"value": world * F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+        host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}
+    else:
+        host = None
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if host is None:
+            host = {n: t.cpu() for n, t in (("q", q), ("k", k), ("v", v), ("kd", kd_raw),
+                                              ("vd", vd_raw))}
+        f, s, rows, threads = oracle_sample(w, host, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} (t, h) rows drawn uniformly from the {w.name} workload (seeded), "
+                      f"{s:.1f} s on {threads} host threads"}
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -27,6 +27,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define MODA_API __attribute__((visibility("default")))
+#else
+#define MODA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -60,7 +66,7 @@ typedef enum {
  * Errors: INVALID_ARG (NULL with L > 0, T < 1, Hk < 1, L < 0, src == dst),
  * UNSUPPORTED (d), MISALIGNED, CUDA.
  */
-moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk,
+MODA_API moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                             int d, moda_stream_t stream);
 
 /*
@@ -91,7 +97,7 @@ moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk,
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA (synchronous);
  * TIMEOUT via moda_get_device_error.
  */
-moda_status moda_fwd(const void* q, const void* k, const void* v,
+MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
                      const void* kd, const void* vd, int T, int Hq, int Hk,
                      int d, int L, float scale, void* o, float* lse,
                      moda_stream_t stream);
@@ -100,14 +106,14 @@ moda_status moda_fwd(const void* q, const void* k, const void* v,
  * moda_get_device_error -- synchronises `stream`, then returns and clears
  * the current device's latched kernel error word (MODA_OK if none).
  */
-moda_status moda_get_device_error(moda_stream_t stream);
+MODA_API moda_status moda_get_device_error(moda_stream_t stream);
 
 /* Static, human-readable name of a status code. */
-const char* moda_status_string(moda_status s);
+MODA_API const char* moda_status_string(moda_status s);
 
 /* Detail of the last non-OK status returned on the calling host thread
  * (which argument, which CUDA error). Never NULL. */
-const char* moda_last_error_detail(void);
+MODA_API const char* moda_last_error_detail(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,175 @@
+// C-ABI entry points of libmoda.so (declared in include/moda.h): argument
+// validation, the per-device kernel error word, and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moda.h"
+#include "moda_internal.h"
+
+// Latched by kernels whose bounded waits give up; read and cleared by
+// moda_get_device_error. One copy per device (module-scope device variable).
+__device__ unsigned int g_moda_err = 0;
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+moda_status fail(moda_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moda_status fail(moda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+moda_status ok() {
+  g_detail[0] = '\0';
+  return MODA_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+// Current device, its error-word address and SM count; checks that it is
+// an sm_103 part (the only target the library is compiled for).
+moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(MODA_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_err_ptr[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3)
+      return fail(MODA_ERR_NO_DEVICE, "device %d is sm_%d%d; libmoda is built for sm_103a", dev,
+                  major, minor);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_moda_err);
+    if (e != cudaSuccess || !p)
+      return fail(MODA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = (unsigned int*)p;
+    g_num_sms[dev] = sms;
+  }
+  *dev_out = dev;
+  *err_out = g_err_ptr[dev];
+  *sms_out = g_num_sms[dev];
+  return MODA_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moda_status_string(moda_status s) {
+  switch (s) {
+    case MODA_OK: return "MODA_OK";
+    case MODA_ERR_INVALID_ARG: return "MODA_ERR_INVALID_ARG";
+    case MODA_ERR_UNSUPPORTED: return "MODA_ERR_UNSUPPORTED";
+    case MODA_ERR_MISALIGNED: return "MODA_ERR_MISALIGNED";
+    case MODA_ERR_CUDA: return "MODA_ERR_CUDA";
+    case MODA_ERR_TIMEOUT: return "MODA_ERR_TIMEOUT";
+    case MODA_ERR_NO_DEVICE: return "MODA_ERR_NO_DEVICE";
+  }
+  return "MODA_ERR_UNKNOWN";
+}
+
+const char* moda_last_error_detail(void) { return g_detail; }
+
+moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk, int d,
+                            moda_stream_t stream) {
+  if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (Hk < 1) return fail(MODA_ERR_INVALID_ARG, "Hk = %d < 1", Hk);
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (L == 0) return ok();
+  if (!src || !dst) return fail(MODA_ERR_INVALID_ARG, "NULL src or dst with L = %d", L);
+  if (!aligned16(src) || !aligned16(dst))
+    return fail(MODA_ERR_MISALIGNED, "src or dst not 16-byte aligned");
+  const size_t bytes = (size_t)L * T * Hk * d * 2;
+  if (overlaps(src, bytes, dst, bytes)) return fail(MODA_ERR_INVALID_ARG, "src and dst overlap");
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_pack_depth(src, dst, L, T, Hk, d, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "pack_depth launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, int T, int Hq, int Hk, int d, int L, float scale, void* o,
+                     float* lse, moda_stream_t stream) {
+  if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL q, k, v or o");
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
+  if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
+  if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
+  if (L > 0 && (!kd || !vd)) return fail(MODA_ERR_INVALID_ARG, "NULL kd or vd with L = %d", L);
+  if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+    return fail(MODA_ERR_INVALID_ARG, "scale is not finite");
+  const int G = Hq / Hk;
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
+  if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (L > 0 && (!aligned16(kd) || !aligned16(vd))) || (lse && !aligned16(lse)))
+    return fail(MODA_ERR_MISALIGNED, "a tensor pointer is not 16-byte aligned");
+  const size_t qb = (size_t)T * Hq * d * 2, kvb = (size_t)T * Hk * d * 2;
+  const size_t db = (size_t)Hk * T * L * d * 2, lb = lse ? (size_t)T * Hq * 4 : 0;
+  const void* ins[5] = {q, k, v, L ? kd : nullptr, L ? vd : nullptr};
+  const size_t insz[5] = {qb, kvb, kvb, db, db};
+  for (int i = 0; i < 5; ++i) {
+    if (overlaps(o, qb, ins[i], insz[i]) || overlaps(lse, lb, ins[i], insz[i]))
+      return fail(MODA_ERR_INVALID_ARG, "an output overlaps an input");
+  }
+  if (overlaps(o, qb, lse, lb)) return fail(MODA_ERR_INVALID_ARG, "o and lse overlap");
+
+  moda::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v;
+  a.kd = L ? kd : nullptr; a.vd = L ? vd : nullptr;
+  a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G;
+  a.scale = scale; a.o = o; a.lse = lse;
+  moda_status st = device_state(&a.device, &a.err, &a.num_sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_fwd_mma(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_fwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_get_device_error(moda_stream_t stream) {
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  unsigned int val = 0;
+  const unsigned int zero = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&val, err, sizeof val, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(err, &zero, sizeof zero, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  if (val != 0) return fail((moda_status)val, "a kernel latched %s", moda_status_string((moda_status)val));
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// Internal declarations shared by the translation units of libmoda.so.
+// Not part of the public ABI (that is include/moda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moda.h"
+
+namespace moda {
+
+// Arguments of one forward call after validation on the host.
+struct FwdArgs {
+  const void* q;   // [T, Hq, d]
+  const void* k;   // [T, Hk, d]
+  const void* v;   // [T, Hk, d]
+  const void* kd;  // [Hk, T, L, d] packed, or nullptr when L == 0
+  const void* vd;  // [Hk, T, L, d] packed, or nullptr when L == 0
+  int T, Hq, Hk, d, L, G;
+  float scale;
+  void* o;         // [T, Hq, d] bf16
+  float* lse;      // [T, Hq] fp32 or nullptr
+  unsigned int* err;  // device error word of the current device
+  int num_sms;
+  int device;
+};
+
+// Kernel error codes latched into the device error word (first one wins).
+enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
+
+// Launchers. Return cudaSuccess or the launch error.
+cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
+                              int d, cudaStream_t stream);
+cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
+
+}  // namespace moda
