@@ -1,0 +1,431 @@
+// MoDA forward on the 5th-generation tensor core (sm_103a): TMA-staged tiles,
+// tcgen05.mma into tensor memory (TMEM), warp-specialised pipeline.
+//
+// What it computes is Mixture-of-Depths Attention, Sec. 2.2 (one softmax over
+// the causal sequence keys of the layer and the L depth slots of the same
+// position), organised as the paper's fused kernel (Sec. 3.3, Algorithm 1):
+//
+//   * group-aware query tile (Sec. 3.2): the M = 128 rows of a tile are 128/G
+//     consecutive positions x the G query heads that share KV head hk, row
+//     r <-> (position p0 + r/G, head hk*G + r%G). One 3-D TMA box over
+//     q[T][Hq][d] lands exactly this stacking, so every K/V block staged in
+//     shared memory serves all G heads;
+//   * depth blocks: the packed depth rows of the tile's positions are one
+//     contiguous run kd[hk][p0 .. p0+128/G)[0..L) (chunk-aware layout), read
+//     128 rows per block; row r keeps depth column j iff floor(j/L) == r/G
+//     (block-diagonal mask of Sec. 3.3). They run FIRST: an exact online
+//     softmax is order-free, and the depth maximum seeds the running max;
+//   * sequence blocks of 128 keys, the grouped causal mask key <= p0 + r/G
+//     applied only on blocks that reach past p0;
+//   * one running state per row: max m (log2 units), sum l, and the
+//     unnormalised output O, which lives in TMEM and is accumulated by the
+//     tensor core; o = O / l once at the end, lse = m ln2 + ln l.
+//
+// Roles (8 warps, one CTA per tile, longest tiles first):
+//   warp 0  lane 0: TMA producer for Q and the K blocks
+//   warp 1  lane 0: tcgen05.mma issuer; the whole warp allocates TMEM
+//   warp 2  lane 0: TMA producer for the V blocks
+//   warps 4-7     : softmax, one thread per tile row (= TMEM lane), and the
+//                   epilogue
+// TMEM (512 columns): S double buffer [0,128) [128,256), O [256, 256+d),
+// P (bf16 pairs) double buffer [384,448) [448,512). The MMA computes
+// S_{j+1} = Q K_{j+1}^T while the softmax turns S_j into P_j, then
+// O += P_j V_j with P read straight from TMEM.
+// The running max is rescaled lazily: O and l are rescaled only when a new
+// block raises the row max by more than 8 (a factor 256), which stays exact
+// because o = O / l uses the same reference for both.
+//
+// Every wait is bounded (2 s); on expiry the CTA stops issuing work, waits
+// for its in-flight copies and MMAs, frees TMEM and latches MODA_ERR_TIMEOUT
+// in the device error word.
+#include <cuda_bf16.h>
+
+#include "moda_internal.h"
+#include "sm103.cuh"
+#include "tensor_map.h"
+
+namespace moda {
+namespace {
+
+using namespace sm103;
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int kThreads = 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;     // 64-column (128-byte) swizzle boxes per row
+  static constexpr int kBoxBytes = 128 * 64 * 2;
+  static constexpr int kNSK = D == 128 ? 3 : 4;  // K stages
+  static constexpr int kNSV = D == 128 ? 2 : 4;  // V stages
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kNSK * kKVBytes;
+  static constexpr int kOffBar = kOffV + kNSV * kKVBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct alignas(8) Barriers {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Barriers) <= 256, "barrier block");
+
+struct Params {
+  int T, Hq, Hk, L, lgG, ntiles;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* err;
+};
+
+// All lanes poll; the warp proceeds only if every lane saw the phase.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKd,
+                   const __grid_constant__ CUtensorMap tmVd, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
+  volatile int* abort = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = 1 << p.lgG;
+  const int P = BM >> p.lgG;  // positions per tile
+  const int tile = p.ntiles - 1 - (int)(blockIdx.x / p.Hk);
+  const int hk = (int)(blockIdx.x % p.Hk);
+  const int p0 = tile * P;
+  const int npos = min(P, p.T - p0);
+  const int t_last = p0 + npos - 1;
+  const int nd = npos * p.L;
+  const int n_depth = (nd + BN - 1) / BN;
+  const int nb = n_depth + t_last / BN + 1;
+  const int depth_row0 = (hk * p.T + p0) * p.L;  // first packed depth row of the tile
+
+  if (tid == 0) {
+    bars->abort = 0;
+    mbar_init(smem_u32(&bars->q_full), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(smem_u32(&bars->k_full[s]), 1);
+      mbar_init(smem_u32(&bars->k_empty[s]), 1);
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->p_full[b]), 128);
+      mbar_init(smem_u32(&bars->pv_done[b]), 1);
+    }
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    if (p.L) {
+      tma_prefetch_desc(&tmKd);
+      tma_prefetch_desc(&tmVd);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------ TMA producers
+    if (lane == 0) {
+      const bool is_k = warp == 0;
+      const int NS = is_k ? C::kNSK : C::kNSV;
+      const uint32_t sbase = is_k ? sK : sV;
+      const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
+      const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      if (is_k) {
+        const uint32_t qb = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qb, C::kQBytes);
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_3d(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0);
+      }
+      int issued = 0;
+      for (int j = 0; j < nb; ++j) {
+        const int s = j % NS;
+        if (!mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs)) break;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::kKVBytes);
+        const uint32_t dst = sbase + s * C::kKVBytes;
+        if (j < n_depth) {
+          for (int c = 0; c < C::kBoxes; ++c)
+            tma_load_2d(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + j * BN);
+        } else {
+          for (int c = 0; c < C::kBoxes; ++c)
+            tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, (j - n_depth) * BN);
+        }
+        issued = j + 1;
+      }
+      // drain: every copy this thread issued has landed before smem is released
+      int never = 0;
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        mbar_wait_bounded(smem_u32(&full[j % NS]), (j / NS) & 1, &never, kTimeoutNs);
+      if (is_k) mbar_wait_bounded(smem_u32(&bars->q_full), 0, &never, kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % C::kNSK;
+        if (!mbar_wait_bounded(smem_u32(&bars->k_full[s]), (j / C::kNSK) & 1, abort, kTimeoutNs))
+          return false;
+        tc_fence_after();
+        const uint32_t kt = sK + s * C::kKVBytes;
+        const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(dcol, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kt + off, 16, 1024), idS,
+                 kk > 0);
+        }
+        tc_commit(smem_u32(&bars->k_empty[s]));
+        tc_commit(smem_u32(&bars->s_full[j & 1]));
+        return true;
+      };
+      bool ok = mbar_wait_bounded(smem_u32(&bars->q_full), 0, abort, kTimeoutNs);
+      if (ok) tc_fence_after();
+      for (int j = 0; ok && j < min(2, nb); ++j) ok = issue_s(j);
+      for (int j = 0; ok && j < nb; ++j) {
+        const int sb = j & 1;
+        if (!mbar_wait_bounded(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, abort, kTimeoutNs)) break;
+        const int vs = j % C::kNSV;
+        if (!mbar_wait_bounded(smem_u32(&bars->v_full[vs]), (j / C::kNSV) & 1, abort, kTimeoutNs))
+          break;
+        tc_fence_after();
+        const uint32_t vt = sV + vs * C::kKVBytes;
+        const uint32_t pcol = tbase + C::kColP + sb * 64;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tbase + C::kColO, pcol + kk * 8, sdesc_sw128(vt + kk * 2048, C::kBoxBytes, 1024),
+                 idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&bars->v_empty[vs]));
+        tc_commit(smem_u32(&bars->pv_done[sb]));
+        if (j + 2 < nb) ok = issue_s(j + 2);
+      }
+      // every MMA issued by this thread has completed before TMEM is freed
+      int never = 0;
+      tc_commit(smem_u32(&bars->mma_done));
+      mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ softmax + epilogue
+    const int row = tid - 128;                 // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
+    const int lp = row >> p.lgG;
+    const int t_row = p0 + lp;
+    const int h_row = hk * G + (row & (G - 1));
+    const bool valid = t_row < p.T;
+    const int t_mask = min(t_row, p.T - 1);
+    const int d_lo = lp * p.L;
+    const int d_hi = min(d_lo + p.L, nd);
+    const float sl = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int sb = j & 1;
+      if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // S row of this thread: 128 fp32 held as raw bits in registers
+      uint32_t x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
+      tmem_ld_wait();
+      const float NEG = -INFINITY;
+      if (j < n_depth) {
+        const int j0 = j * BN;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int jd = j0 + c;
+          x[c] = __float_as_uint((jd >= d_lo && jd < d_hi) ? __uint_as_float(x[c]) * sl : NEG);
+        }
+      } else {
+        const int k0 = (j - n_depth) * BN;
+        if (k0 + BN - 1 > p0) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            x[c] = __float_as_uint((k0 + c <= t_mask) ? __uint_as_float(x[c]) * sl : NEG);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * sl);
+        }
+      }
+      float mx = __uint_as_float(x[0]);
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
+      const bool need = mx > m_ref + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_ref;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+        if (j > 0) {
+          // O holds blocks 0..j-1: wait for the last of them, then rescale it
+          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
+            tmem_ld32(ta, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(ta, r);
+          }
+          tmem_st_wait();
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sum = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN / 2; ++c) {
+        const float e0 = ex2_approx(__uint_as_float(x[2 * c]) - base);
+        const float e1 = ex2_approx(__uint_as_float(x[2 * c + 1]) - base);
+        sum += e0 + e1;
+        pk[c] = pack_bf16x2(e0, e1);
+      }
+      l += sum;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c)
+        tmem_st32(tmem_addr(tbase, lane_base, C::kColP + sb * 64 + c * 32), pk + c * 32);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->p_full[sb]));
+    }
+    if (ok) {
+      ok = warp_wait(smem_u32(&bars->pv_done[(nb - 1) & 1]), ((nb - 1) >> 1) & 1, abort);
+      if (ok && nb >= 2)
+        ok = warp_wait(smem_u32(&bars->pv_done[(nb - 2) & 1]), ((nb - 2) >> 1) & 1, abort);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, C::kColO + c * 32), r);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+  if (tid == 0 && bars->abort) atomicCAS(p.err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
+  using C = Cfg<D>;
+  const int lgG = __builtin_ctz((unsigned)a.G);
+  const int P = BM >> lgG;
+  const int ntiles = (a.T + P - 1) / P;
+  CUtensorMap tq, tk, tv, tkd, tvd;
+  const uint64_t row = (uint64_t)D * 2;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hq};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)P};
+    if (encode_bf16_sw128(&tq, a.q, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hk};
+    const uint32_t box[3] = {64, 1, BN};
+    if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  if (a.L > 0) {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
+    const uint64_t str[1] = {row};
+    const uint32_t box[2] = {64, BN};
+    if (encode_bf16_sw128(&tkd, a.kd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  } else {
+    tkd = tk;  // never read when L == 0
+    tvd = tv;
+  }
+  Params prm;
+  prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.ntiles = ntiles;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.o = (__nv_bfloat16*)a.o;
+  prm.lse = a.lse;
+  prm.err = a.err;
+  cudaError_t e = cudaFuncSetAttribute(moda_fwd_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = (int64_t)ntiles * a.Hk;
+  moda_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tkd, tvd, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
+}
+
+}  // namespace moda

@@ -131,6 +131,9 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
     return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
   if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
   if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if ((int64_t)Hk * T * L > 0x7fffffffLL)
+    return fail(MODA_ERR_UNSUPPORTED, "Hk*T*L = %lld packed depth rows exceed 2^31 - 1",
+                (long long)Hk * T * L);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (L > 0 && (!aligned16(kd) || !aligned16(vd))) || (lse && !aligned16(lse)))
     return fail(MODA_ERR_MISALIGNED, "a tensor pointer is not 16-byte aligned");
@@ -151,7 +154,7 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   a.scale = scale; a.o = o; a.lse = lse;
   moda_status st = device_state(&a.device, &a.err, &a.num_sms);
   if (st != MODA_OK) return st;
-  cudaError_t e = moda::launch_fwd_mma(a, (cudaStream_t)stream);
+  cudaError_t e = moda::launch_fwd_tc(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_fwd launch: %s", cudaGetErrorString(e));
   return ok();
 }

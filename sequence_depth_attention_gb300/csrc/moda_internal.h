@@ -32,5 +32,6 @@ enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
 
 }  // namespace moda
