@@ -19,8 +19,7 @@
  *     that gave up) is latched in a per-device error word and reported by
  *     moda_get_device_error().
  *   - Batch is 1; callers loop over sequences.
- *   - Thread safety: calls may be made from several host threads; the
- *     tensor-map cache is guarded by a mutex.
+ *   - Thread safety: calls may be made from several host threads.
  */
 #ifndef MODA_H_
 #define MODA_H_
@@ -86,7 +85,8 @@ MODA_API moda_status moda_pack_depth(const void* src, void* dst, int L, int T, i
  *   k, v    [T, Hk, d] bf16
  *   kd, vd  [Hk, T, L, d] bf16, the PACKED depth stream (moda_pack_depth);
  *           may be NULL when L == 0, which makes the call plain causal GQA
- *   scale   the logit scale, usually 1/sqrt(d); used for sequence and depth
+ *   scale   the logit scale, > 0 and finite, usually 1/sqrt(d); used for
+ *           sequence and depth logits alike
  *   o       [T, Hq, d] bf16 output, rounded to nearest even
  *   lse     [T, Hq] fp32 output (may be NULL if not wanted)
  * Arithmetic: bf16 products, fp32 accumulation, softmax in fp32 through exp2

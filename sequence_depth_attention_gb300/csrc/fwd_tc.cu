@@ -268,34 +268,50 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         break;
       }
       tc_fence_after();
-      // S row of this thread: 128 fp32 held as raw bits in registers
+      // S row of this thread: 128 raw fp32 scores held as bits in registers
       uint32_t x[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
         tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
       tmem_ld_wait();
-      const float NEG = -INFINITY;
-      if (j < n_depth) {
-        const int j0 = j * BN;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int jd = j0 + c;
-          x[c] = __float_as_uint((jd >= d_lo && jd < d_hi) ? __uint_as_float(x[c]) * sl : NEG);
+      // mask on raw scores: keep columns [lo, hi) of this block (scale > 0, so
+      // masking and the max commute with scaling)
+      {
+        int lo = 0, hi = BN;
+        if (j < n_depth) {
+          lo = d_lo - j * BN;
+          hi = d_hi - j * BN;
+        } else {
+          const int k0 = (j - n_depth) * BN;
+          if (k0 + BN - 1 > p0) hi = t_mask - k0 + 1;
         }
-      } else {
-        const int k0 = (j - n_depth) * BN;
-        if (k0 + BN - 1 > p0) {
+        lo = max(lo, 0);
+        hi = min(hi, BN);
+        if (lo > 0 || hi < BN) {
+          const unsigned span = (unsigned)max(hi - lo, 0);
 #pragma unroll
           for (int c = 0; c < BN; ++c)
-            x[c] = __float_as_uint((k0 + c <= t_mask) ? __uint_as_float(x[c]) * sl : NEG);
-        } else {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * sl);
+            x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;  // -inf
         }
       }
-      float mx = __uint_as_float(x[0]);
+      // row max: three-input max tree, depth 4
+      float mx;
+      {
+        float a1[43];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
+        for (int i = 0; i < 42; ++i)
+          a1[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]),
+                        __uint_as_float(x[3 * i + 2]));
+        a1[42] = fmaxf(__uint_as_float(x[126]), __uint_as_float(x[127]));
+        float a2[15];
+#pragma unroll
+        for (int i = 0; i < 14; ++i) a2[i] = max3f(a1[3 * i], a1[3 * i + 1], a1[3 * i + 2]);
+        a2[14] = a1[42];
+        float a3[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
+        mx = fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
+      }
       const bool need = mx > m_ref + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_ref;
@@ -322,17 +338,30 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         l *= alpha;
         m_ref = m_new;
       }
-      const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
+      // p = 2^(s*sl - m): one packed FMA per pair, then the exponential unit
+      const float nbase = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
       uint32_t pk[BN / 2];
+      uint64_t ps[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float e0 = ex2_approx(__uint_as_float(x[2 * c]) - base);
-        const float e1 = ex2_approx(__uint_as_float(x[2 * c + 1]) - base);
-        sum += e0 + e1;
+        float u, w;
+        f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2), u, w);
+        const float e0 = ex2_approx(u), e1 = ex2_approx(w);
         pk[c] = pack_bf16x2(e0, e1);
+        ps[c] = f2(e0, e1);
       }
-      l += sum;
+      // row sum: packed pairwise tree
+#pragma unroll
+      for (int w = BN / 4; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int c = 0; c < w; ++c) ps[c] = fadd2(ps[c], ps[c + w]);
+      }
+      {
+        float u, w;
+        f2_split(ps[0], u, w);
+        l += u + w;
+      }
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c)
         tmem_st32(tmem_addr(tbase, lane_base, C::kColP + sb * 64 + c * 32), pk + c * 32);

@@ -123,8 +123,8 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
   if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
   if (L > 0 && (!kd || !vd)) return fail(MODA_ERR_INVALID_ARG, "NULL kd or vd with L = %d", L);
-  if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
-    return fail(MODA_ERR_INVALID_ARG, "scale is not finite");
+  if (!(scale > 0.f) || scale == __builtin_inff())
+    return fail(MODA_ERR_INVALID_ARG, "scale must be positive and finite");
   const int G = Hq / Hk;
   if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)

@@ -70,6 +70,7 @@ def fwd(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.12
     (dict(T=0), INVALID), (dict(T=-5), INVALID), (dict(L=-1), INVALID),
     (dict(Hq=5, Hk=2), INVALID), (dict(Hk=0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(scale=0.0), INVALID), (dict(scale=-0.125), INVALID),
     (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
     (dict(Hq=6, Hk=2), UNSUPPORTED), (dict(Hq=64, Hk=2), UNSUPPORTED),
     (dict(T=(1 << 24) + 1), UNSUPPORTED), (dict(L=1025), UNSUPPORTED),
