@@ -182,6 +182,20 @@ def oracle_sample(w, host, rows_budget_s, seed=0, nthreads=None):
         batch = min(batch * 2, max(nthreads, int(rows * (rows_budget_s - el) / max(el, 1e-3))))
 
 
+def max_over_ranks(val, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (identity on one rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(val)
+    t = torch.tensor([float(val)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, ms_per_step, world):
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def host_inputs(w):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     x = wl.make_inputs(w, device=dev)
@@ -192,7 +206,8 @@ def run_reference(args, w, rank):
     if rank != 0:
         return
     host = host_inputs(w)
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = args.cpu_seconds if args.cpu_seconds_set else \
+        max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
         oracle_sample(w, host, per_step, seed=1000 + i)
     flops = secs = 0.0
@@ -228,7 +243,7 @@ def config_of(w, n):
 
 
 # ----------------------------------------------------------------- GPU arm
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
@@ -237,8 +252,13 @@ def main():
     ap.add_argument("--workload", default=wl.LONG.name)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    args = ap.parse_args()
+    ap.add_argument("--cpu-seconds", type=float, default=None,
+                    help="seconds of oracle work for cpu_baseline (default 10) or per "
+                         "reference-arm step (default: sized to the run)")
+    args = ap.parse_args(argv)
+    args.cpu_seconds_set = args.cpu_seconds is not None
+    if args.cpu_seconds is None:
+        args.cpu_seconds = 10.0
     if args.warmup < 3 and args.impl == "moda":
         print("note: warm-up raised to the minimum of 3", file=sys.stderr)
         args.warmup = 3
@@ -297,13 +317,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(val):
-        if dist is None:
-            return val
-        t = torch.tensor([val], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     for _ in range(W):
         step()
     st = moda.moda_get_device_error(stream)
@@ -321,7 +334,7 @@ def main():
     end.record(stream)
     barrier()
     clk = clocks.stop()
-    ms_step = max_over_ranks(start.elapsed_time(end) / K)
+    ms_step = max_over_ranks(start.elapsed_time(end) / K, dist, dev)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
     pack_ms = statistics.mean(a.elapsed_time(b) for a, b in pack_ev)
     st = moda.moda_get_device_error(stream)
@@ -344,7 +357,7 @@ def main():
 
     peaks, peaks_src = load_peaks()
     F = w.flops()
-    value = world * F / (ms_step * 1e-3) / 1e12
+    value = job_tflops(F, ms_step, world)
     fwd_tflops = F / (fwd_ms * 1e-3) / 1e12
     fwd0_tflops = w0.flops() / (fwd0_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
@@ -403,11 +416,11 @@ def main():
             e2e_step()
         b.record(stream)
         barrier()
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / K)
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / K, dist, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv)) + \
             (sum(t.numel() * t.element_size() for t in (hkd, hvd)) if w.L else 0)
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        line["e2e"] = {"value": world * F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        line["e2e"] = {"value": job_tflops(F, e2e_ms, world), "unit": "TFLOP/s",
                        "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h}
         host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}

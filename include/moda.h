@@ -108,6 +108,17 @@ MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
  */
 MODA_API moda_status moda_get_device_error(moda_stream_t stream);
 
+/*
+ * moda_selftest_wait_timeout -- diagnostic of the failure path; the paper has
+ * no counterpart. Launches one thread that waits, through the same bounded
+ * shared-memory-barrier wait the forward kernel uses, on a barrier nothing
+ * ever arrives on. After timeout_ms (1..5000) the wait gives up and latches
+ * MODA_ERR_TIMEOUT in the device error word, as a stalled forward pipeline
+ * would; the kernel returns normally and the context stays usable. Read the
+ * result with moda_get_device_error. Errors: INVALID_ARG (timeout_ms), CUDA.
+ */
+MODA_API moda_status moda_selftest_wait_timeout(int timeout_ms, moda_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 MODA_API const char* moda_status_string(moda_status s);
 

@@ -25,7 +25,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
 
 # every symbol include/moda.h declares
 EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_get_device_error",
-           "moda_status_string", "moda_last_error_detail")
+           "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +59,8 @@ def load():
         lib.moda_fwd.restype = i
         lib.moda_get_device_error.argtypes = [vp]
         lib.moda_get_device_error.restype = i
+        lib.moda_selftest_wait_timeout.argtypes = [i, vp]
+        lib.moda_selftest_wait_timeout.restype = i
         lib.moda_status_string.argtypes = [i]
         lib.moda_status_string.restype = ctypes.c_char_p
         lib.moda_last_error_detail.argtypes = []
@@ -147,3 +149,10 @@ def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
 def moda_get_device_error(stream=None) -> int:
     """Synchronise the stream; return and clear the device's kernel error word."""
     return int(load().moda_get_device_error(_stream(stream)))
+
+
+def moda_selftest_wait_timeout(timeout_ms: int = 50, stream=None) -> None:
+    """Launch the failure-path diagnostic; read its latched status with
+    moda_get_device_error()."""
+    _check(load().moda_selftest_wait_timeout(int(timeout_ms), _stream(stream)),
+           "moda_selftest_wait_timeout")

@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;     // 64-column (128-byte) swizzle boxes per row
   static constexpr int kBoxBytes = 128 * 64 * 2;
   static constexpr int kNSK = D == 128 ? 3 : 4;  // K stages
-  static constexpr int kNSV = D == 128 ? 2 : 4;  // V stages
+  static constexpr int kNSV = D == 128 ? 3 : 4;  // V stages
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kOffQ = 0;
@@ -78,7 +78,7 @@ struct alignas(8) Barriers {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -138,6 +138,7 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->s_free[b]), 128);
       mbar_init(smem_u32(&bars->p_full[b]), 128);
       mbar_init(smem_u32(&bars->pv_done[b]), 1);
     }
@@ -164,24 +165,28 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------ TMA producers
-    if (lane == 0) {
-      const bool is_k = warp == 0;
-      const int NS = is_k ? C::kNSK : C::kNSV;
-      const uint32_t sbase = is_k ? sK : sV;
-      const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
-      const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
-      uint64_t* full = is_k ? bars->k_full : bars->v_full;
-      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
-      if (is_k) {
-        const uint32_t qb = smem_u32(&bars->q_full);
-        mbar_arrive_expect_tx(qb, C::kQBytes);
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0);
-      }
-      int issued = 0;
-      for (int j = 0; j < nb; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs)) break;
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues the copies.
+    const bool leader = elect_one();
+    const bool is_k = warp == 0;
+    const int NS = is_k ? C::kNSK : C::kNSV;
+    const uint32_t sbase = is_k ? sK : sV;
+    const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
+    const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
+    uint64_t* full = is_k ? bars->k_full : bars->v_full;
+    uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    if (is_k && leader) {
+      const uint32_t qb = smem_u32(&bars->q_full);
+      mbar_arrive_expect_tx(qb, C::kQBytes);
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_3d(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0);
+    }
+    int issued = 0;
+    for (int j = 0; j < nb; ++j) {
+      const int s = j % NS;
+      const bool ok = mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (leader) {
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::kKVBytes);
         const uint32_t dst = sbase + s * C::kKVBytes;
@@ -192,61 +197,88 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           for (int c = 0; c < C::kBoxes; ++c)
             tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, (j - n_depth) * BN);
         }
-        issued = j + 1;
       }
-      // drain: every copy this thread issued has landed before smem is released
+      __syncwarp();
+      issued = j + 1;
+    }
+    // drain: every copy this warp issued has landed before smem is released
+    if (leader) {
       int never = 0;
       for (int j = max(0, issued - NS); j < issued; ++j)
         mbar_wait_bounded(smem_u32(&full[j % NS]), (j / NS) & 1, &never, kTimeoutNs);
       if (is_k) mbar_wait_bounded(smem_u32(&bars->q_full), 0, &never, kTimeoutNs);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % C::kNSK;
-        if (!mbar_wait_bounded(smem_u32(&bars->k_full[s]), (j / C::kNSK) & 1, abort, kTimeoutNs))
-          return false;
-        tc_fence_after();
-        const uint32_t kt = sK + s * C::kKVBytes;
+    // The whole warp follows the pipeline so descriptors stay warp-uniform;
+    // one elected lane issues tcgen05.mma / tcgen05.commit.
+    const bool leader = elect_one();
+    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
+    // base descriptors; the start-address field (bits 0-13, 16-byte units)
+    // is advanced by adding byte offsets >> 4
+    const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+      return __all_sync(0xffffffffu, ok);
+    };
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % C::kNSK;
+      if (!wait(&bars->k_full[s], (j / C::kNSK) & 1)) return false;
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dks = dk + (uint64_t)((s * C::kKVBytes) >> 4);
         const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(dcol, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kt + off, 16, 1024), idS,
-                 kk > 0);
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(dcol, dq + off, dks + off, idS, kk > 0);
         }
         tc_commit(smem_u32(&bars->k_empty[s]));
         tc_commit(smem_u32(&bars->s_full[j & 1]));
-        return true;
-      };
-      bool ok = mbar_wait_bounded(smem_u32(&bars->q_full), 0, abort, kTimeoutNs);
-      if (ok) tc_fence_after();
-      for (int j = 0; ok && j < min(2, nb); ++j) ok = issue_s(j);
-      for (int j = 0; ok && j < nb; ++j) {
-        const int sb = j & 1;
-        if (!mbar_wait_bounded(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, abort, kTimeoutNs)) break;
-        const int vs = j % C::kNSV;
-        if (!mbar_wait_bounded(smem_u32(&bars->v_full[vs]), (j / C::kNSV) & 1, abort, kTimeoutNs))
-          break;
+      }
+      __syncwarp();
+      return true;
+    };
+    // Issue order: S_0, S_1, then per block j: S_{j+2} as soon as the
+    // softmax has read S_j out of its buffer, and PV_j once P_j is ready.
+    // S_{j+2} thus runs on the tensor core while the softmax works on j.
+    bool ok = wait(&bars->q_full, 0);
+    if (ok) tc_fence_after();
+    for (int j = 0; ok && j < min(2, nb); ++j) ok = issue_s(j);
+    for (int j = 0; ok && j < nb; ++j) {
+      const int sb = j & 1;
+      if (j + 2 < nb) {
+        if (!wait(&bars->s_free[sb], (j >> 1) & 1)) break;
         tc_fence_after();
-        const uint32_t vt = sV + vs * C::kKVBytes;
+        if (!issue_s(j + 2)) break;
+      }
+      if (!wait(&bars->p_full[sb], (j >> 1) & 1)) break;
+      const int vs = j % C::kNSV;
+      if (!wait(&bars->v_full[vs], (j / C::kNSV) & 1)) break;
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dvs = dv + (uint64_t)((vs * C::kKVBytes) >> 4);
         const uint32_t pcol = tbase + C::kColP + sb * 64;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase + C::kColO, pcol + kk * 8, sdesc_sw128(vt + kk * 2048, C::kBoxBytes, 1024),
-                 idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::kColO, pcol + kk * 8, dvs + (uint64_t)((kk * 2048) >> 4), idPV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(smem_u32(&bars->v_empty[vs]));
         tc_commit(smem_u32(&bars->pv_done[sb]));
-        if (j + 2 < nb) ok = issue_s(j + 2);
       }
-      // every MMA issued by this thread has completed before TMEM is freed
+      __syncwarp();
+    }
+    // every MMA issued by this warp has completed before TMEM is freed
+    if (leader) {
       int never = 0;
       tc_commit(smem_u32(&bars->mma_done));
       mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------ softmax + epilogue
     const int row = tid - 128;                 // tile row == TMEM lane
@@ -274,6 +306,9 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       for (int c = 0; c < BN / 32; ++c)
         tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
       tmem_ld_wait();
+      // S_j is in registers: its TMEM buffer may take S_{j+2}
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->s_free[sb]));
       // mask on raw scores: keep columns [lo, hi) of this block (scale > 0, so
       // masking and the max commute with scaling)
       {
@@ -361,6 +396,14 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         float u, w;
         f2_split(ps[0], u, w);
         l += u + w;
+      }
+      // P_j reuses the buffer of P_{j-2}: the tensor core must have consumed it
+      if (j >= 2) {
+        if (!warp_wait(smem_u32(&bars->pv_done[sb]), ((j - 2) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c)

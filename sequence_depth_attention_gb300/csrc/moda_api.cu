@@ -159,6 +159,18 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   return ok();
 }
 
+moda_status moda_selftest_wait_timeout(int timeout_ms, moda_stream_t stream) {
+  if (timeout_ms < 1 || timeout_ms > 5000)
+    return fail(MODA_ERR_INVALID_ARG, "timeout_ms = %d (allowed 1..5000)", timeout_ms);
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_selftest_wait(err, timeout_ms, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 moda_status moda_get_device_error(moda_stream_t stream) {
   int dev, sms;
   unsigned int* err;

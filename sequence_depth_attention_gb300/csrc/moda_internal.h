@@ -33,5 +33,6 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);
 
 }  // namespace moda

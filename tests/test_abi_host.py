@@ -128,3 +128,8 @@ def test_product_package_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
                 assert "moda_oracle" not in text, f
+
+
+@pytest.mark.parametrize("ms", [0, -1, 5001])
+def test_selftest_rejects_timeout(lib, ms):
+    assert lib.moda_selftest_wait_timeout(ms, None) == INVALID
