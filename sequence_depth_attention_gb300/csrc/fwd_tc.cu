@@ -225,10 +225,15 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
       return __all_sync(0xffffffffu, ok);
     };
-    auto issue_s = [&](int j) -> bool {
+    // Two barriers checked in one round trip: lanes 0-15 poll a, 16-31 poll b.
+    auto wait2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) -> bool {
+      const bool lo = lane < 16;
+      const bool ok = mbar_wait_bounded(smem_u32(lo ? a : b), lo ? pa : pb, abort, kTimeoutNs);
+      return __all_sync(0xffffffffu, ok);
+    };
+    // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
+    auto issue_s = [&](int j) {
       const int s = j % C::kNSK;
-      if (!wait(&bars->k_full[s], (j / C::kNSK) & 1)) return false;
-      tc_fence_after();
       if (leader) {
         const uint64_t dks = dk + (uint64_t)((s * C::kKVBytes) >> 4);
         const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
@@ -241,24 +246,33 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_commit(smem_u32(&bars->s_full[j & 1]));
       }
       __syncwarp();
-      return true;
     };
     // Issue order: S_0, S_1, then per block j: S_{j+2} as soon as the
     // softmax has read S_j out of its buffer, and PV_j once P_j is ready.
     // S_{j+2} thus runs on the tensor core while the softmax works on j.
-    bool ok = wait(&bars->q_full, 0);
-    if (ok) tc_fence_after();
-    for (int j = 0; ok && j < min(2, nb); ++j) ok = issue_s(j);
+    bool ok = wait2(&bars->q_full, 0, &bars->k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+    }
+    if (ok && nb > 1) {
+      ok = wait(&bars->k_full[1 % C::kNSK], (1 / C::kNSK) & 1);
+      if (ok) {
+        tc_fence_after();
+        issue_s(1);
+      }
+    }
     for (int j = 0; ok && j < nb; ++j) {
       const int sb = j & 1;
       if (j + 2 < nb) {
-        if (!wait(&bars->s_free[sb], (j >> 1) & 1)) break;
+        const int ks = (j + 2) % C::kNSK;
+        if (!wait2(&bars->s_free[sb], (j >> 1) & 1, &bars->k_full[ks], ((j + 2) / C::kNSK) & 1))
+          break;
         tc_fence_after();
-        if (!issue_s(j + 2)) break;
+        issue_s(j + 2);
       }
-      if (!wait(&bars->p_full[sb], (j >> 1) & 1)) break;
       const int vs = j % C::kNSV;
-      if (!wait(&bars->v_full[vs], (j / C::kNSV) & 1)) break;
+      if (!wait2(&bars->p_full[sb], (j >> 1) & 1, &bars->v_full[vs], (j / C::kNSV) & 1)) break;
       tc_fence_after();
       if (leader) {
         const uint64_t dvs = dv + (uint64_t)((vs * C::kKVBytes) >> 4);
@@ -329,9 +343,8 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;  // -inf
         }
       }
-      // row max: three-input max tree, depth 4
-      float mx;
-      {
+      // row max of the raw scores (scaled after): three-input max tree, depth 4
+      auto row_max = [&]() -> float {
         float a1[43];
 #pragma unroll
         for (int i = 0; i < 42; ++i)
@@ -345,58 +358,74 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         float a3[5];
 #pragma unroll
         for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
-        mx = fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
-      }
-      const bool need = mx > m_ref + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mx : m_ref;
-        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-        if (j > 0) {
-          // O holds blocks 0..j-1: wait for the last of them, then rescale it
-          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
-            tmem_ld32(ta, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(ta, r);
-          }
-          tmem_st_wait();
-        }
-        l *= alpha;
-        m_ref = m_new;
-      }
-      // p = 2^(s*sl - m): one packed FMA per pair, then the exponential unit
-      const float nbase = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
+        return fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
+      };
+      // p = 2^(s*sl - m) as bf16 pairs into pk; returns the fp32 row sum.
+      // One packed FMA per pair, then the exponential unit; packed-add tree.
       uint32_t pk[BN / 2];
-      uint64_t ps[BN / 2];
+      auto compute_p = [&](float m) -> float {
+        const float nbase = (m == -INFINITY) ? 0.f : -m;
+        const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
+        uint64_t acc[8];
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
+        for (int c = 0; c < BN / 2; ++c) {
+          float u, w;
+          f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2),
+                   u, w);
+          const float e0 = ex2_approx(u), e1 = ex2_approx(w);
+          pk[c] = pack_bf16x2(e0, e1);
+          acc[c & 7] = c < 8 ? f2(e0, e1) : fadd2(acc[c & 7], f2(e0, e1));
+        }
+        acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+        acc[4] = fadd2(fadd2(acc[4], acc[5]), fadd2(acc[6], acc[7]));
+        acc[0] = fadd2(acc[0], acc[4]);
         float u, w;
-        f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2), u, w);
-        const float e0 = ex2_approx(u), e1 = ex2_approx(w);
-        pk[c] = pack_bf16x2(e0, e1);
-        ps[c] = f2(e0, e1);
+        f2_split(acc[0], u, w);
+        return u + w;
+      };
+      // Fast path: exponentiate against the running reference m_ref right
+      // away and check the block max in the shadow of the exponentials. Only
+      // if some row of the warp has no reference yet, or its max rose by more
+      // than the threshold, fall back to max-first with a rescale of O and l.
+      // The max tree comes first in program order but nothing in the fast
+      // path's exponentials depends on it, so the two interleave.
+      const float mx = row_max();
+      float sum = 0.f;
+      bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+      if (!slow) {
+        sum = compute_p(m_ref);
+        slow = __any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold);
       }
-      // row sum: packed pairwise tree
+      if (slow) {
+        const bool need = mx > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mx : m_ref;
+          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+          if (j > 0) {
+            // O holds blocks 0..j-1: wait for the last of them, then rescale it
+            if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-      for (int w = BN / 4; w >= 1; w >>= 1) {
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < w; ++c) ps[c] = fadd2(ps[c], ps[c + w]);
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(ta, r);
+            }
+            tmem_st_wait();
+          }
+          l *= alpha;
+          m_ref = m_new;
+        }
+        sum = compute_p(m_ref);
       }
-      {
-        float u, w;
-        f2_split(ps[0], u, w);
-        l += u + w;
-      }
+      l += sum;
       // P_j reuses the buffer of P_{j-2}: the tensor core must have consumed it
       if (j >= 2) {
         if (!warp_wait(smem_u32(&bars->pv_done[sb]), ((j - 2) >> 1) & 1, abort)) {
