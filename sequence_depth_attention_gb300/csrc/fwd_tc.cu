@@ -13,8 +13,10 @@
 //   * depth blocks: the packed depth rows of the tile's positions are one
 //     contiguous run kd[hk][p0 .. p0+128/G)[0..L) (chunk-aware layout), read
 //     128 rows per block; row r keeps depth column j iff floor(j/L) == r/G
-//     (block-diagonal mask of Sec. 3.3). They run FIRST: an exact online
-//     softmax is order-free, and the depth maximum seeds the running max;
+//     (block-diagonal mask of Sec. 3.3). An exact online softmax does not
+//     depend on block order, so depth blocks are spread evenly among the
+//     sequence blocks: each tile streams its depth rows from HBM over its
+//     lifetime instead of all CTAs of a wave reading them at once;
 //   * sequence blocks of 128 keys, the grouped causal mask key <= p0 + r/G
 //     applied only on blocks that reach past p0;
 //   * one running state per row: max m (log2 units), sum l, and the
@@ -126,6 +128,26 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int n_depth = (nd + BN - 1) / BN;
   const int nb = n_depth + t_last / BN + 1;
   const int depth_row0 = (hk * p.T + p0) * p.L;  // first packed depth row of the tile
+  // Block schedule: the n_depth depth blocks are spread evenly among the
+  // sequence blocks (Bresenham: block j is a depth block iff
+  // floor((j+1)*n_depth/nb) > floor(j*n_depth/nb)), so each tile streams its
+  // depth rows from HBM over its whole lifetime instead of in one burst.
+  // Every role walks the blocks in order with its own Sched copy.
+  struct Sched {
+    int acc = 0, db = 0, sbk = 0;  // remainder, depth blocks so far, sequence blocks so far
+    bool depth = false;            // is the current block a depth block
+    int index = 0;                 // its index among blocks of its kind
+    __device__ void next(int n_depth, int nb) {
+      acc += n_depth;
+      depth = acc >= nb;
+      if (depth) {
+        acc -= nb;
+        index = db++;
+      } else {
+        index = sbk++;
+      }
+    }
+  };
 
   if (tid == 0) {
     bars->abort = 0;
@@ -182,7 +204,9 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tma_load_3d(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0);
     }
     int issued = 0;
+    Sched sch;
     for (int j = 0; j < nb; ++j) {
+      sch.next(n_depth, nb);
       const int s = j % NS;
       const bool ok = mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -190,12 +214,12 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::kKVBytes);
         const uint32_t dst = sbase + s * C::kKVBytes;
-        if (j < n_depth) {
+        if (sch.depth) {
           for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_2d(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + j * BN);
+            tma_load_2d(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + sch.index * BN);
         } else {
           for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, (j - n_depth) * BN);
+            tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, sch.index * BN);
         }
       }
       __syncwarp();
@@ -307,7 +331,9 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const float sl = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    Sched sch;
     for (int j = 0; j < nb; ++j) {
+      sch.next(n_depth, nb);
       const int sb = j & 1;
       if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort)) {
         ok = false;
@@ -327,11 +353,11 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // masking and the max commute with scaling)
       {
         int lo = 0, hi = BN;
-        if (j < n_depth) {
-          lo = d_lo - j * BN;
-          hi = d_hi - j * BN;
+        if (sch.depth) {
+          lo = d_lo - sch.index * BN;
+          hi = d_hi - sch.index * BN;
         } else {
-          const int k0 = (j - n_depth) * BN;
+          const int k0 = sch.index * BN;
           if (k0 + BN - 1 > p0) hi = t_mask - k0 + 1;
         }
         lo = max(lo, 0);
