@@ -197,11 +197,15 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
     uint64_t* full = is_k ? bars->k_full : bars->v_full;
     uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    // Q and the depth rows are read once: evict them first so they do not
+    // push the K/V blocks that later tiles of the head re-read out of L2
+    // (K/V keep the default policy; pinning all of them measured slower).
+    const uint64_t pol_once = l2_policy_evict_first();
     if (is_k && leader) {
       const uint32_t qb = smem_u32(&bars->q_full);
       mbar_arrive_expect_tx(qb, C::kQBytes);
       for (int c = 0; c < C::kBoxes; ++c)
-        tma_load_3d(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0);
+        tma_load_3d_hint(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0, pol_once);
     }
     int issued = 0;
     Sched sch;
@@ -216,7 +220,8 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const uint32_t dst = sbase + s * C::kKVBytes;
         if (sch.depth) {
           for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_2d(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + sch.index * BN);
+            tma_load_2d_hint(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + sch.index * BN,
+                             pol_once);
         } else {
           for (int c = 0; c < C::kBoxes; ++c)
             tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, sch.index * BN);
