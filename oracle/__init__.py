@@ -96,6 +96,8 @@ class Oracle:
         lib.moda_oracle_rows.argtypes = [u16p] * 5 + [i] * 5 + [
             ctypes.c_double, i64p, i64p, ctypes.c_int64, f64p, f64p, i]
         lib.moda_oracle_rows.restype = ctypes.c_int
+        lib.moda_oracle_bwd.argtypes = [u16p] * 6 + [i] * 5 + [ctypes.c_double] + [f64p] * 5 + [i]
+        lib.moda_oracle_bwd.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -150,6 +152,29 @@ class Oracle:
         return o.reshape(T, Hq, d), lse.reshape(T, Hq)
 
 
+    def backward(self, q, k, v, kd, vd, dO, scale, nthreads: int = 1):
+        """All gradients of the forward for upstream gradient dO[T,Hq,d]
+        (bf16 bits). Returns float64 (dq[T,Hq,d], dk[T,Hk,d], dv[T,Hk,d],
+        dkd[L,T,Hk,d], dvd[L,T,Hk,d]); the depth gradients are in the
+        unpacked append layout."""
+        arrs, (T, Hq, Hk, d, L) = self._prep(q, k, v, kd, vd)
+        dO = _u16(dO, "dO")
+        if dO.shape != (T, Hq, d):
+            raise ValueError("dO must be [T,Hq,d]")
+        dq = np.zeros((T, Hq, d))
+        dk = np.zeros((T, Hk, d))
+        dv = np.zeros((T, Hk, d))
+        dkd = np.zeros((L, T, Hk, d))
+        dvd = np.zeros((L, T, Hk, d))
+        p = lambda a: _ptr(a, ctypes.c_double) if a.size else None
+        rc = self._lib.moda_oracle_bwd(
+            *(_ptr(a, ctypes.c_uint16) for a in arrs), _ptr(dO, ctypes.c_uint16),
+            T, Hq, Hk, d, L, float(scale), p(dq), p(dk), p(dv), p(dkd), p(dvd), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"moda_oracle_bwd failed with {rc}")
+        return dq, dk, dv, dkd, dvd
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -168,3 +193,7 @@ def rows(*args, **kw):
 
 def forward(*args, **kw):
     return default().forward(*args, **kw)
+
+
+def backward(*args, **kw):
+    return default().backward(*args, **kw)

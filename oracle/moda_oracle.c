@@ -178,3 +178,162 @@ int moda_oracle_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   free(th);
   return status;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward of the joint-softmax forward above, fp64, one query row at a time
+ * (the gradient of the MoDA forward of Sec. 2.2 with respect to every input;
+ * the pages time forward + backward in Table 2 and Table 7 but do not spell
+ * the backward out, so this is the chain rule through the definition):
+ *
+ *   for row (t, h) with joint row z, p = softmax(z), o = sum_c p_c val_c:
+ *     D      = <dO[t,h,:], o>
+ *     dp_c   = <dO[t,h,:], val_c>
+ *     ds_c   = p_c (dp_c - D)              (gradient w.r.t. z_c)
+ *     dq[t,h]        += scale * sum_c ds_c key_c
+ *     dk[j,hk]       += scale * ds_j q[t,h]        j <= t
+ *     dv[j,hk]       += p_j dO[t,h]
+ *     dkd[l,t,hk]    += scale * ds_{t+1+l} q[t,h]  (same position only)
+ *     dvd[l,t,hk]    += p_{t+1+l} dO[t,h]
+ *
+ * dO is bf16 bits like the other inputs; every gradient is double. The depth
+ * gradients use the UNPACKED layout [L, T, Hk, d]. Rows are split over
+ * threads; each thread accumulates dk/dv/dkd/dvd privately and the copies are
+ * summed in thread order, so results do not depend on scheduling.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const uint16_t *q, *k, *v, *kd, *vd, *dO;
+  int T, Hq, Hk, d, L;
+  double scale;
+  int64_t begin, end; /* row range, row = t*Hq + h */
+  double *dq, *dk, *dv, *dkd, *dvd; /* dq shared (rows disjoint), rest private */
+  int status;
+} bwd_job;
+
+static void* bwd_worker(void* arg) {
+  bwd_job* jb = (bwd_job*)arg;
+  const int T = jb->T, Hq = jb->Hq, Hk = jb->Hk, d = jb->d, L = jb->L;
+  const int G = Hq / Hk;
+  double* z = (double*)malloc(((size_t)T + L) * sizeof(double));
+  double* o = (double*)malloc((size_t)d * sizeof(double));
+  double* g = (double*)malloc((size_t)d * sizeof(double));
+  double* qr = (double*)malloc((size_t)d * sizeof(double));
+  jb->status = 0;
+  if (!z || !o || !g || !qr) {
+    jb->status = -2;
+    free(z); free(o); free(g); free(qr);
+    return NULL;
+  }
+  for (int64_t row = jb->begin; row < jb->end; ++row) {
+    const int t = (int)(row / Hq), h = (int)(row % Hq), hk = h / G;
+    const uint16_t* qrow = jb->q + row * d;
+    const uint16_t* dorow = jb->dO + row * d;
+    for (int c = 0; c < d; ++c) {
+      qr[c] = bf16_to_double(qrow[c]);
+      g[c] = bf16_to_double(dorow[c]);
+    }
+    const int64_t n = (int64_t)t + 1 + L;
+    for (int64_t j = 0; j <= t; ++j) z[j] = jb->scale * dot_bf16(qrow, jb->k + (j * Hk + hk) * d, d);
+    for (int l = 0; l < L; ++l)
+      z[t + 1 + l] = jb->scale * dot_bf16(qrow, jb->kd + (((int64_t)l * T + t) * Hk + hk) * d, d);
+    double m = z[0];
+    for (int64_t j = 1; j < n; ++j)
+      if (z[j] > m) m = z[j];
+    double Z = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      z[j] = exp(z[j] - m);
+      Z += z[j];
+    }
+    for (int64_t j = 0; j < n; ++j) z[j] /= Z; /* z now holds p */
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      const uint16_t* val = j <= t ? jb->v + (j * Hk + hk) * d
+                                   : jb->vd + (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
+      for (int c = 0; c < d; ++c) o[c] += z[j] * bf16_to_double(val[c]);
+    }
+    double D = 0.0;
+    for (int c = 0; c < d; ++c) D += g[c] * o[c];
+    double* dqr = jb->dq + row * d;
+    for (int64_t j = 0; j < n; ++j) {
+      const int is_seq = j <= t;
+      const int64_t kv_off = is_seq ? (j * Hk + hk) * d
+                                    : (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
+      const uint16_t* key = (is_seq ? jb->k : jb->kd) + kv_off;
+      const uint16_t* val = (is_seq ? jb->v : jb->vd) + kv_off;
+      double dp = 0.0;
+      for (int c = 0; c < d; ++c) dp += g[c] * bf16_to_double(val[c]);
+      const double p = z[j];
+      const double ds = p * (dp - D);
+      double* dkey = (is_seq ? jb->dk : jb->dkd) + kv_off;
+      double* dval = (is_seq ? jb->dv : jb->dvd) + kv_off;
+      for (int c = 0; c < d; ++c) {
+        dqr[c] += jb->scale * ds * bf16_to_double(key[c]);
+        dkey[c] += jb->scale * ds * qr[c];
+        dval[c] += p * g[c];
+      }
+    }
+  }
+  free(z); free(o); free(g); free(qr);
+  return NULL;
+}
+
+/* All gradients of the forward: dq[T,Hq,d], dk/dv[T,Hk,d], dkd/dvd[L,T,Hk,d]
+ * (double, overwritten). kd/vd/dkd/dvd may be NULL when L == 0. */
+int moda_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const uint16_t* kd, const uint16_t* vd, const uint16_t* dO, int T, int Hq,
+                    int Hk, int d, int L, double scale, double* dq, double* dk, double* dv,
+                    double* dkd, double* dvd, int nthreads) {
+  if (T < 1 || Hq < 1 || Hk < 1 || d < 1 || L < 0 || Hq % Hk != 0) return -1;
+  if (L > 0 && (!kd || !vd || !dkd || !dvd)) return -1;
+  const int64_t rows = (int64_t)T * Hq;
+  const size_t nq = (size_t)rows * d, nk = (size_t)T * Hk * d, nd = (size_t)L * T * Hk * d;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > rows) nthreads = (int)rows;
+  bwd_job* jobs = (bwd_job*)calloc((size_t)nthreads, sizeof(bwd_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  double* priv = (double*)calloc((size_t)nthreads * (2 * nk + 2 * nd), sizeof(double));
+  if (!jobs || !th || !priv) {
+    free(jobs); free(th); free(priv);
+    return -2;
+  }
+  memset(dq, 0, nq * sizeof(double));
+  for (int i = 0; i < nthreads; ++i) {
+    bwd_job* jb = &jobs[i];
+    double* base = priv + (size_t)i * (2 * nk + 2 * nd);
+    jb->q = q; jb->k = k; jb->v = v; jb->kd = kd; jb->vd = vd; jb->dO = dO;
+    jb->T = T; jb->Hq = Hq; jb->Hk = Hk; jb->d = d; jb->L = L; jb->scale = scale;
+    jb->begin = rows * i / nthreads;
+    jb->end = rows * (i + 1) / nthreads;
+    jb->dq = dq;
+    jb->dk = base; jb->dv = base + nk; jb->dkd = base + 2 * nk; jb->dvd = base + 2 * nk + nd;
+  }
+  int started = 0;
+  for (int i = 1; i < nthreads; ++i) {
+    if (pthread_create(&th[i], NULL, bwd_worker, &jobs[i]) != 0) break;
+    ++started;
+  }
+  bwd_worker(&jobs[0]);
+  for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+  for (int i = started + 1; i < nthreads; ++i) bwd_worker(&jobs[i]);
+  int status = 0;
+  for (int i = 0; i < nthreads && status == 0; ++i) status = jobs[i].status;
+  memset(dk, 0, nk * sizeof(double));
+  memset(dv, 0, nk * sizeof(double));
+  if (L > 0) {
+    memset(dkd, 0, nd * sizeof(double));
+    memset(dvd, 0, nd * sizeof(double));
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    const bwd_job* jb = &jobs[i];
+    for (size_t e = 0; e < nk; ++e) {
+      dk[e] += jb->dk[e];
+      dv[e] += jb->dv[e];
+    }
+    for (size_t e = 0; e < nd; ++e) {
+      dkd[e] += jb->dkd[e];
+      dvd[e] += jb->dvd[e];
+    }
+  }
+  free(jobs); free(th); free(priv);
+  return status;
+}

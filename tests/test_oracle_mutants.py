@@ -14,12 +14,12 @@ MUTANTS = {
     "self_key_dropped": ("z[j] = scale * dot_bf16(qrow, krow, d);",
                          "z[j] = (j == t) ? -1e300 : scale * dot_bf16(qrow, krow, d);"),
     "head_mod_not_div": ("const int hk = h / G;", "const int hk = h % Hk;"),
-    "depth_index_swapped": ("kd + (((int64_t)l * T + t) * Hk + hk) * d",
-                            "kd + (((int64_t)t * L + l) * Hk + hk) * d"),
+    "depth_index_swapped": ("const uint16_t* kdrow = kd + (((int64_t)l * T + t) * Hk + hk) * d;",
+                            "const uint16_t* kdrow = kd + (((int64_t)t * L + l) * Hk + hk) * d;"),
     "depth_scale_dropped": ("z[t + 1 + l] = scale * dot_bf16(qrow, kdrow, d);",
                             "z[t + 1 + l] = dot_bf16(qrow, kdrow, d);"),
     "depth_value_from_keys": ("const uint16_t* vdrow = vd +", "const uint16_t* vdrow = kd +"),
-    "exp_sign_flipped": ("z[j] = exp(z[j] - m);", "z[j] = exp(m - z[j]);"),
+    "exp_sign_flipped": ("z[j] = exp(z[j] - m); /* z now holds", "z[j] = exp(m - z[j]); /* z now holds"),
     "lse_without_max": ("*lse = m + log(Z);", "*lse = log(Z);"),
     "depth_previous_position": ("const uint16_t* kdrow = kd + (((int64_t)l * T + t) * Hk + hk) * d;",
                                 "const uint16_t* kdrow = kd + (((int64_t)l * T + (t > 0 ? t - 1 : t)) * Hk + hk) * d;"),
