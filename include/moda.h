@@ -103,6 +103,38 @@ MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
                      moda_stream_t stream);
 
 /*
+ * moda_bwd -- gradients of moda_fwd with respect to all of its inputs. The
+ * pages time the fused operator forward + backward (Table 2, Table 7) without
+ * writing the backward out; this is the chain rule through the joint softmax
+ * of Sec. 2.2. For row (t, h) with probabilities p_c over its candidates c
+ * (keys j <= t, then the L depth slots of position t):
+ *   D = <dO[t,h], o[t,h]>,  dp_c = <dO[t,h], val_c>,  ds_c = p_c (dp_c - D)
+ *   dq[t,h]  = scale * sum_c ds_c key_c
+ *   dk[j,hk] = scale * sum of ds_j q[t,h] over the rows that see key j
+ *   dv[j,hk] = sum of p_j dO[t,h] over those rows
+ *   dkd[hk,t,l], dvd[hk,t,l]: the same for slot l, from the G rows of position t
+ *
+ *   q, k, v, kd, vd, scale  exactly as passed to moda_fwd (kd/vd packed)
+ *   o       [T, Hq, d] bf16   the forward output
+ *   lse     [T, Hq] fp32      the forward log-sum-exp (natural log)
+ *   dO      [T, Hq, d] bf16   gradient of the loss with respect to o
+ *   dq      [T, Hq, d] fp32   outputs, overwritten
+ *   dk, dv  [T, Hk, d] fp32
+ *   dkd, dvd [Hk, T, L, d] fp32 (packed, like kd/vd); may be NULL when L == 0
+ *   delta   [T, Hq] fp32      workspace owned by the caller; holds D on return
+ * Arithmetic: bf16 operands, fp32 accumulation; P and dS are rounded to bf16
+ * as tensor-core operands. No atomics: results are deterministic.
+ * Outputs and the workspace must not overlap the inputs or each other.
+ * Same supported shapes as moda_fwd. Errors: INVALID_ARG, UNSUPPORTED,
+ * MISALIGNED, CUDA.
+ */
+MODA_API moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd,
+                              const void* vd, const void* o, const float* lse, const void* dO,
+                              int T, int Hq, int Hk, int d, int L, float scale, float* dq,
+                              float* dk, float* dv, float* dkd, float* dvd, float* delta,
+                              moda_stream_t stream);
+
+/*
  * moda_get_device_error -- synchronises `stream`, then returns and clears
  * the current device's latched kernel error word (MODA_OK if none).
  */

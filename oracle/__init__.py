@@ -98,6 +98,9 @@ class Oracle:
         lib.moda_oracle_rows.restype = ctypes.c_int
         lib.moda_oracle_bwd.argtypes = [u16p] * 6 + [i] * 5 + [ctypes.c_double] + [f64p] * 5 + [i]
         lib.moda_oracle_bwd.restype = ctypes.c_int
+        lib.moda_oracle_bwd_rows.argtypes = [u16p] * 6 + [i] * 5 + [ctypes.c_double, i64p,
+                                              ctypes.c_int64, i] + [f64p] * 5 + [i]
+        lib.moda_oracle_bwd_rows.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -172,6 +175,28 @@ class Oracle:
             T, Hq, Hk, d, L, float(scale), p(dq), p(dk), p(dv), p(dkd), p(dvd), int(nthreads))
         if rc != 0:
             raise ValueError(f"moda_oracle_bwd failed with {rc}")
+        return dq, dk, dv, dkd, dvd
+
+
+    def backward_rows(self, q, k, v, kd, vd, dO, scale, rows, k_lo, nthreads: int = 1):
+        """Gradient contributions of the rows listed (row = t*Hq + h): returns
+        (dq_rows[n,d], dk_tail[T-k_lo,Hk,d], dv_tail, dkd_rows[n,L,d], dvd_rows)."""
+        arrs, (T, Hq, Hk, d, L) = self._prep(q, k, v, kd, vd)
+        dO = _u16(dO, "dO")
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+        n = rows.shape[0]
+        dq = np.zeros((n, d))
+        dk = np.zeros((T - k_lo, Hk, d))
+        dv = np.zeros((T - k_lo, Hk, d))
+        dkd = np.zeros((n, L, d))
+        dvd = np.zeros((n, L, d))
+        p = lambda a: _ptr(a, ctypes.c_double) if a.size else None
+        rc = self._lib.moda_oracle_bwd_rows(
+            *(_ptr(a, ctypes.c_uint16) for a in arrs), _ptr(dO, ctypes.c_uint16),
+            T, Hq, Hk, d, L, float(scale), _ptr(rows, ctypes.c_int64), n, int(k_lo),
+            p(dq), p(dk), p(dv), p(dkd), p(dvd), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"moda_oracle_bwd_rows failed with {rc}")
         return dq, dk, dv, dkd, dvd
 
 

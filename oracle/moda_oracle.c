@@ -200,12 +200,88 @@ int moda_oracle_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * threads; each thread accumulates dk/dv/dkd/dvd privately and the copies are
  * summed in thread order, so results do not depend on scheduling.
  * ------------------------------------------------------------------------ */
+/* Where one row's gradient contributions go. Sequence key j >= k_lo lands at
+ * dk + ((j - k_lo)*Hk + hk)*d (keys below k_lo are not accumulated); depth
+ * slot l lands at dkd_row + l*dkd_stride. */
+typedef struct {
+  double *dq_row, *dk, *dv, *dkd_row, *dvd_row;
+  int k_lo;
+  int64_t dkd_stride;
+} bwd_dst;
+
+/* Gradient contributions of query row (t, h); work buffers z[T+L], o, g, qr[d]. */
+static void bwd_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const uint16_t* kd, const uint16_t* vd, const uint16_t* dO, int T, int Hq,
+                    int Hk, int d, int L, double scale, int t, int h, const bwd_dst* dst,
+                    double* z, double* o, double* g, double* qr) {
+  const int G = Hq / Hk, hk = h / G;
+  const int64_t row = (int64_t)t * Hq + h;
+  const uint16_t* qrow = q + row * d;
+  const uint16_t* dorow = dO + row * d;
+  for (int c = 0; c < d; ++c) {
+    qr[c] = bf16_to_double(qrow[c]);
+    g[c] = bf16_to_double(dorow[c]);
+  }
+  const int64_t n = (int64_t)t + 1 + L;
+  for (int64_t j = 0; j <= t; ++j) z[j] = scale * dot_bf16(qrow, k + (j * Hk + hk) * d, d);
+  for (int l = 0; l < L; ++l)
+    z[t + 1 + l] = scale * dot_bf16(qrow, kd + (((int64_t)l * T + t) * Hk + hk) * d, d);
+  double m = z[0];
+  for (int64_t j = 1; j < n; ++j)
+    if (z[j] > m) m = z[j];
+  double Z = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    z[j] = exp(z[j] - m);
+    Z += z[j];
+  }
+  for (int64_t j = 0; j < n; ++j) z[j] /= Z; /* z now holds p */
+  for (int c = 0; c < d; ++c) o[c] = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    const uint16_t* val = j <= t ? v + (j * Hk + hk) * d
+                                 : vd + (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
+    for (int c = 0; c < d; ++c) o[c] += z[j] * bf16_to_double(val[c]);
+  }
+  double D = 0.0;
+  for (int c = 0; c < d; ++c) D += g[c] * o[c];
+  for (int64_t j = 0; j < n; ++j) {
+    const int is_seq = j <= t;
+    const int64_t kv_off = is_seq ? (j * Hk + hk) * d
+                                  : (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
+    const uint16_t* key = (is_seq ? k : kd) + kv_off;
+    const uint16_t* val = (is_seq ? v : vd) + kv_off;
+    double dp = 0.0;
+    for (int c = 0; c < d; ++c) dp += g[c] * bf16_to_double(val[c]);
+    const double p = z[j];
+    const double ds = p * (dp - D);
+    double *dkey = NULL, *dval = NULL;
+    if (is_seq) {
+      if (j >= dst->k_lo) {
+        dkey = dst->dk + ((j - dst->k_lo) * Hk + hk) * d;
+        dval = dst->dv + ((j - dst->k_lo) * Hk + hk) * d;
+      }
+    } else if (dst->dkd_row) {
+      dkey = dst->dkd_row + (j - t - 1) * dst->dkd_stride;
+      dval = dst->dvd_row + (j - t - 1) * dst->dkd_stride;
+    }
+    for (int c = 0; c < d; ++c) {
+      dst->dq_row[c] += scale * ds * bf16_to_double(key[c]);
+      if (dkey) {
+        dkey[c] += scale * ds * qr[c];
+        dval[c] += p * g[c];
+      }
+    }
+  }
+}
+
 typedef struct {
   const uint16_t *q, *k, *v, *kd, *vd, *dO;
   int T, Hq, Hk, d, L;
   double scale;
-  int64_t begin, end; /* row range, row = t*Hq + h */
-  double *dq, *dk, *dv, *dkd, *dvd; /* dq shared (rows disjoint), rest private */
+  const int64_t* rows; /* row = t*Hq + h; NULL means rows begin..end-1 */
+  int64_t begin, end;
+  int k_lo;
+  int rows_mode;       /* 0: full layouts; 1: per-row depth outputs, dk/dv tail */
+  double *dq, *dk, *dv, *dkd, *dvd; /* dq (and per-row depth) disjoint; dk/dv private */
   int status;
 } bwd_job;
 
@@ -223,61 +299,52 @@ static void* bwd_worker(void* arg) {
     free(z); free(o); free(g); free(qr);
     return NULL;
   }
-  for (int64_t row = jb->begin; row < jb->end; ++row) {
+  for (int64_t i = jb->begin; i < jb->end; ++i) {
+    const int64_t row = jb->rows ? jb->rows[i] : i;
     const int t = (int)(row / Hq), h = (int)(row % Hq), hk = h / G;
-    const uint16_t* qrow = jb->q + row * d;
-    const uint16_t* dorow = jb->dO + row * d;
-    for (int c = 0; c < d; ++c) {
-      qr[c] = bf16_to_double(qrow[c]);
-      g[c] = bf16_to_double(dorow[c]);
+    bwd_dst dst;
+    dst.k_lo = jb->k_lo;
+    dst.dk = jb->dk;
+    dst.dv = jb->dv;
+    if (jb->rows_mode) {
+      dst.dq_row = jb->dq + i * d;
+      dst.dkd_row = L ? jb->dkd + i * (int64_t)L * d : NULL;
+      dst.dvd_row = L ? jb->dvd + i * (int64_t)L * d : NULL;
+      dst.dkd_stride = d;
+    } else {
+      dst.dq_row = jb->dq + row * d;
+      dst.dkd_row = L ? jb->dkd + ((int64_t)t * Hk + hk) * d : NULL;
+      dst.dvd_row = L ? jb->dvd + ((int64_t)t * Hk + hk) * d : NULL;
+      dst.dkd_stride = (int64_t)T * Hk * d;
     }
-    const int64_t n = (int64_t)t + 1 + L;
-    for (int64_t j = 0; j <= t; ++j) z[j] = jb->scale * dot_bf16(qrow, jb->k + (j * Hk + hk) * d, d);
-    for (int l = 0; l < L; ++l)
-      z[t + 1 + l] = jb->scale * dot_bf16(qrow, jb->kd + (((int64_t)l * T + t) * Hk + hk) * d, d);
-    double m = z[0];
-    for (int64_t j = 1; j < n; ++j)
-      if (z[j] > m) m = z[j];
-    double Z = 0.0;
-    for (int64_t j = 0; j < n; ++j) {
-      z[j] = exp(z[j] - m);
-      Z += z[j];
-    }
-    for (int64_t j = 0; j < n; ++j) z[j] /= Z; /* z now holds p */
-    for (int c = 0; c < d; ++c) o[c] = 0.0;
-    for (int64_t j = 0; j < n; ++j) {
-      const uint16_t* val = j <= t ? jb->v + (j * Hk + hk) * d
-                                   : jb->vd + (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
-      for (int c = 0; c < d; ++c) o[c] += z[j] * bf16_to_double(val[c]);
-    }
-    double D = 0.0;
-    for (int c = 0; c < d; ++c) D += g[c] * o[c];
-    double* dqr = jb->dq + row * d;
-    for (int64_t j = 0; j < n; ++j) {
-      const int is_seq = j <= t;
-      const int64_t kv_off = is_seq ? (j * Hk + hk) * d
-                                    : (((int64_t)(j - t - 1) * T + t) * Hk + hk) * d;
-      const uint16_t* key = (is_seq ? jb->k : jb->kd) + kv_off;
-      const uint16_t* val = (is_seq ? jb->v : jb->vd) + kv_off;
-      double dp = 0.0;
-      for (int c = 0; c < d; ++c) dp += g[c] * bf16_to_double(val[c]);
-      const double p = z[j];
-      const double ds = p * (dp - D);
-      double* dkey = (is_seq ? jb->dk : jb->dkd) + kv_off;
-      double* dval = (is_seq ? jb->dv : jb->dvd) + kv_off;
-      for (int c = 0; c < d; ++c) {
-        dqr[c] += jb->scale * ds * bf16_to_double(key[c]);
-        dkey[c] += jb->scale * ds * qr[c];
-        dval[c] += p * g[c];
-      }
-    }
+    bwd_row(jb->q, jb->k, jb->v, jb->kd, jb->vd, jb->dO, T, Hq, Hk, d, L, jb->scale, t, h, &dst,
+            z, o, g, qr);
   }
   free(z); free(o); free(g); free(qr);
   return NULL;
 }
 
+/* Runs jobs[0..nthreads) (job 0 on the calling thread); returns the first error. */
+static int run_bwd_jobs(bwd_job* jobs, int nthreads) {
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!th) return -2;
+  int started = 0;
+  for (int i = 1; i < nthreads; ++i) {
+    if (pthread_create(&th[i], NULL, bwd_worker, &jobs[i]) != 0) break;
+    ++started;
+  }
+  bwd_worker(&jobs[0]);
+  for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+  for (int i = started + 1; i < nthreads; ++i) bwd_worker(&jobs[i]);
+  free(th);
+  int status = 0;
+  for (int i = 0; i < nthreads && status == 0; ++i) status = jobs[i].status;
+  return status;
+}
+
 /* All gradients of the forward: dq[T,Hq,d], dk/dv[T,Hk,d], dkd/dvd[L,T,Hk,d]
- * (double, overwritten). kd/vd/dkd/dvd may be NULL when L == 0. */
+ * (double, overwritten). kd/vd/dkd/dvd may be NULL when L == 0. Every thread
+ * accumulates dk/dv/dkd/dvd privately; the copies are summed in thread order. */
 int moda_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     const uint16_t* kd, const uint16_t* vd, const uint16_t* dO, int T, int Hq,
                     int Hk, int d, int L, double scale, double* dq, double* dk, double* dv,
@@ -290,10 +357,9 @@ int moda_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   if (nthreads > 256) nthreads = 256;
   if ((int64_t)nthreads > rows) nthreads = (int)rows;
   bwd_job* jobs = (bwd_job*)calloc((size_t)nthreads, sizeof(bwd_job));
-  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
   double* priv = (double*)calloc((size_t)nthreads * (2 * nk + 2 * nd), sizeof(double));
-  if (!jobs || !th || !priv) {
-    free(jobs); free(th); free(priv);
+  if (!jobs || !priv) {
+    free(jobs); free(priv);
     return -2;
   }
   memset(dq, 0, nq * sizeof(double));
@@ -302,21 +368,15 @@ int moda_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     double* base = priv + (size_t)i * (2 * nk + 2 * nd);
     jb->q = q; jb->k = k; jb->v = v; jb->kd = kd; jb->vd = vd; jb->dO = dO;
     jb->T = T; jb->Hq = Hq; jb->Hk = Hk; jb->d = d; jb->L = L; jb->scale = scale;
+    jb->rows = NULL;
     jb->begin = rows * i / nthreads;
     jb->end = rows * (i + 1) / nthreads;
+    jb->k_lo = 0;
+    jb->rows_mode = 0;
     jb->dq = dq;
     jb->dk = base; jb->dv = base + nk; jb->dkd = base + 2 * nk; jb->dvd = base + 2 * nk + nd;
   }
-  int started = 0;
-  for (int i = 1; i < nthreads; ++i) {
-    if (pthread_create(&th[i], NULL, bwd_worker, &jobs[i]) != 0) break;
-    ++started;
-  }
-  bwd_worker(&jobs[0]);
-  for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
-  for (int i = started + 1; i < nthreads; ++i) bwd_worker(&jobs[i]);
-  int status = 0;
-  for (int i = 0; i < nthreads && status == 0; ++i) status = jobs[i].status;
+  const int status = run_bwd_jobs(jobs, nthreads);
   memset(dk, 0, nk * sizeof(double));
   memset(dv, 0, nk * sizeof(double));
   if (L > 0) {
@@ -334,6 +394,65 @@ int moda_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
       dvd[e] += jb->dvd[e];
     }
   }
-  free(jobs); free(th); free(priv);
+  free(jobs); free(priv);
+  return status;
+}
+
+/* Gradient contributions of the listed rows only (row = t*Hq + h):
+ *   dq_rows[i][:]                 dq of row i (complete)
+ *   dkd_rows[i][l][:], dvd_rows   row i's share of the depth gradients of its
+ *                                 position (the sum over the G heads of a
+ *                                 position is the full depth gradient there)
+ *   dk_tail[j-k_lo][hk][:], dv_tail  the listed rows' share of the gradients
+ *                                 of keys k_lo <= j < T (complete when every
+ *                                 row of positions >= k_lo is listed)
+ * Used to check large workloads without an O(T^2) full backward. */
+int moda_oracle_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const uint16_t* kd, const uint16_t* vd, const uint16_t* dO, int T,
+                         int Hq, int Hk, int d, int L, double scale, const int64_t* rows,
+                         int64_t n, int k_lo, double* dq_rows, double* dk_tail, double* dv_tail,
+                         double* dkd_rows, double* dvd_rows, int nthreads) {
+  if (T < 1 || Hq < 1 || Hk < 1 || d < 1 || L < 0 || Hq % Hk != 0 || n < 0) return -1;
+  if (k_lo < 0 || k_lo > T) return -1;
+  if (L > 0 && (!kd || !vd || !dkd_rows || !dvd_rows)) return -1;
+  for (int64_t i = 0; i < n; ++i)
+    if (rows[i] < 0 || rows[i] >= (int64_t)T * Hq) return -1;
+  const size_t nk = (size_t)(T - k_lo) * Hk * d;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+  bwd_job* jobs = (bwd_job*)calloc((size_t)nthreads, sizeof(bwd_job));
+  double* priv = (double*)calloc((size_t)nthreads * 2 * (nk ? nk : 1), sizeof(double));
+  if (!jobs || !priv) {
+    free(jobs); free(priv);
+    return -2;
+  }
+  memset(dq_rows, 0, (size_t)n * d * sizeof(double));
+  if (L > 0) {
+    memset(dkd_rows, 0, (size_t)n * L * d * sizeof(double));
+    memset(dvd_rows, 0, (size_t)n * L * d * sizeof(double));
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    bwd_job* jb = &jobs[i];
+    jb->q = q; jb->k = k; jb->v = v; jb->kd = kd; jb->vd = vd; jb->dO = dO;
+    jb->T = T; jb->Hq = Hq; jb->Hk = Hk; jb->d = d; jb->L = L; jb->scale = scale;
+    jb->rows = rows;
+    jb->begin = n * i / nthreads;
+    jb->end = n * (i + 1) / nthreads;
+    jb->k_lo = k_lo;
+    jb->rows_mode = 1;
+    jb->dq = dq_rows; jb->dkd = dkd_rows; jb->dvd = dvd_rows;
+    jb->dk = priv + (size_t)i * 2 * (nk ? nk : 1);
+    jb->dv = jb->dk + nk;
+  }
+  const int status = run_bwd_jobs(jobs, nthreads);
+  memset(dk_tail, 0, nk * sizeof(double));
+  memset(dv_tail, 0, nk * sizeof(double));
+  for (int i = 0; i < nthreads; ++i)
+    for (size_t e = 0; e < nk; ++e) {
+      dk_tail[e] += jobs[i].dk[e];
+      dv_tail[e] += jobs[i].dv[e];
+    }
+  free(jobs); free(priv);
   return status;
 }

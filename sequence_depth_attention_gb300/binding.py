@@ -24,7 +24,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_get_device_error",
+EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_bwd", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
@@ -57,6 +57,8 @@ def load():
         lib.moda_pack_depth.restype = i
         lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd.restype = i
+        lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
+        lib.moda_bwd.restype = i
         lib.moda_get_device_error.argtypes = [vp]
         lib.moda_get_device_error.restype = i
         lib.moda_selftest_wait_timeout.argtypes = [i, vp]
@@ -144,6 +146,39 @@ def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
                          float(scale), _ptr(o), _ptr(lse), _stream(stream))
     _check(st, "moda_fwd")
     return o, lse
+
+
+def moda_bwd(q, k, v, kd, vd, o, lse, dO, scale: float, grads=None, delta=None, stream=None):
+    """Gradients of moda_fwd. Inputs as passed to moda_fwd plus the forward's
+    o and lse and the upstream gradient dO[T,Hq,d] (bf16). Returns fp32
+    (dq[T,Hq,d], dk[T,Hk,d], dv[T,Hk,d], dkd[Hk,T,L,d], dvd[Hk,T,L,d]) with
+    the depth gradients in the packed layout (None when L == 0)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _need(t, n)
+    _need(lse, "lse", torch.float32)
+    T, Hq, d = q.shape
+    Hk = k.shape[1]
+    L = 0 if kd is None or kd.numel() == 0 else kd.shape[2]
+    if L:
+        _need(kd, "kd"), _need(vd, "vd")
+    dev = q.device
+    if grads is None:
+        f32 = dict(dtype=torch.float32, device=dev)
+        grads = (torch.empty((T, Hq, d), **f32), torch.empty((T, Hk, d), **f32),
+                 torch.empty((T, Hk, d), **f32),
+                 torch.empty((Hk, T, L, d), **f32) if L else None,
+                 torch.empty((Hk, T, L, d), **f32) if L else None)
+    if delta is None:
+        delta = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    dq, dk, dv, dkd, dvd = grads
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv"), (delta, "delta")):
+        _need(t, n, torch.float32)
+    st = load().moda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kd if L else None),
+                         _ptr(vd if L else None), _ptr(o), _ptr(lse), _ptr(dO), T, Hq, Hk, d, L,
+                         float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkd if L else None),
+                         _ptr(dvd if L else None), _ptr(delta), _stream(stream))
+    _check(st, "moda_bwd")
+    return dq, dk, dv, dkd, dvd
 
 
 def moda_get_device_error(stream=None) -> int:

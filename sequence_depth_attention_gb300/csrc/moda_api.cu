@@ -159,6 +159,59 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   return ok();
 }
 
+moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd, const void* vd,
+                     const void* o, const float* lse, const void* dO, int T, int Hq, int Hk,
+                     int d, int L, float scale, float* dq, float* dk, float* dv, float* dkd,
+                     float* dvd, float* delta, moda_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
+    return fail(MODA_ERR_INVALID_ARG, "NULL input, output or workspace pointer");
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
+  if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
+  if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
+  if (L > 0 && (!kd || !vd || !dkd || !dvd))
+    return fail(MODA_ERR_INVALID_ARG, "NULL kd, vd, dkd or dvd with L = %d", L);
+  if (!(scale > 0.f) || scale == __builtin_inff())
+    return fail(MODA_ERR_INVALID_ARG, "scale must be positive and finite");
+  const int G = Hq / Hk;
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
+  if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  const void* all[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, L ? kd : nullptr, L ? vd : nullptr,
+                       L ? dkd : nullptr, L ? dvd : nullptr};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return fail(MODA_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  const size_t qb = (size_t)T * Hq * d * 2, kvb = (size_t)T * Hk * d * 2;
+  const size_t db = (size_t)Hk * T * L * d * 2, lb = (size_t)T * Hq * 4;
+  const void* ins[] = {q, k, v, L ? kd : nullptr, L ? vd : nullptr, o, lse, dO};
+  const size_t insz[] = {qb, kvb, kvb, db, db, qb, lb, qb};
+  void* outs[] = {dq, dk, dv, L ? dkd : nullptr, L ? dvd : nullptr, delta};
+  const size_t outsz[] = {2 * qb, 2 * kvb, 2 * kvb, 2 * db, 2 * db, lb};
+  for (int a = 0; a < 6; ++a) {
+    for (int b = 0; b < 8; ++b)
+      if (overlaps(outs[a], outsz[a], ins[b], insz[b]))
+        return fail(MODA_ERR_INVALID_ARG, "an output or the workspace overlaps an input");
+    for (int b = a + 1; b < 6; ++b)
+      if (overlaps(outs[a], outsz[a], outs[b], outsz[b]))
+        return fail(MODA_ERR_INVALID_ARG, "two outputs overlap");
+  }
+  moda::BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.kd = L ? kd : nullptr; a.vd = L ? vd : nullptr;
+  a.o = o; a.dO = dO; a.lse = lse;
+  a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G; a.scale = scale;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dkd = L ? dkd : nullptr; a.dvd = L ? dvd : nullptr;
+  a.delta = delta;
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_bwd(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_bwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 moda_status moda_selftest_wait_timeout(int timeout_ms, moda_stream_t stream) {
   if (timeout_ms < 1 || timeout_ms > 5000)
     return fail(MODA_ERR_INVALID_ARG, "timeout_ms = %d (allowed 1..5000)", timeout_ms);

@@ -25,6 +25,16 @@ struct FwdArgs {
   int device;
 };
 
+// Arguments of one backward call after validation on the host.
+struct BwdArgs {
+  const void *q, *k, *v, *kd, *vd, *o, *dO;  // bf16; kd/vd packed, nullptr when L == 0
+  const float* lse;                          // [T, Hq]
+  int T, Hq, Hk, d, L, G;
+  float scale;
+  float *dq, *dk, *dv, *dkd, *dvd;           // fp32 outputs (dkd/dvd packed)
+  float* delta;                              // [T, Hq] caller workspace
+};
+
 // Kernel error codes latched into the device error word (first one wins).
 enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 
@@ -33,6 +43,7 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);
 
 }  // namespace moda

@@ -44,9 +44,9 @@ BWD_MUTANTS = {
     "missing_D_term": ("const double ds = p * (dp - D);", "const double ds = p * dp;"),
     "ds_sign": ("const double ds = p * (dp - D);", "const double ds = p * (D - dp);"),
     "dv_uses_ds": ("dval[c] += p * g[c];", "dval[c] += ds * g[c];"),
-    "dk_no_scale": ("dkey[c] += jb->scale * ds * qr[c];", "dkey[c] += ds * qr[c];"),
-    "dq_uses_values": ("dqr[c] += jb->scale * ds * bf16_to_double(key[c]);",
-                       "dqr[c] += jb->scale * ds * bf16_to_double(val[c]);"),
+    "dk_no_scale": ("dkey[c] += scale * ds * qr[c];", "dkey[c] += ds * qr[c];"),
+    "dq_uses_values": ("dst->dq_row[c] += scale * ds * bf16_to_double(key[c]);",
+                       "dst->dq_row[c] += scale * ds * bf16_to_double(val[c]);"),
     "D_from_dO_squared": ("for (int c = 0; c < d; ++c) D += g[c] * o[c];",
                           "for (int c = 0; c < d; ++c) D += g[c] * g[c];"),
 }
@@ -62,3 +62,26 @@ def test_bwd_pins_catch_mutant(tmp_path, name):
     orc = oracle.Oracle(oracle.build(force=True, src=str(path), out=str(tmp_path / "libm.so")))
     failed = [n for n, (err, tol) in pins_bwd.run_all(orc).items() if not err <= tol]
     assert failed, f"no backward pin catches mutant {name}"
+
+
+def test_bwd_rows_matches_full(orc):
+    """The row-subset backward reproduces the full one: dq rows, depth
+    gradients summed over the heads of each position, and the tail keys."""
+    from sequence_depth_attention_gb300.inputs import bf16_bits
+    T, Hq, Hk, d, L = 40, 8, 2, 8, 5
+    x, dO = pins_bwd.case(T, Hq, Hk, d, L, 53)
+    b = {n: bf16_bits(t) for n, t in x.items()}
+    full = orc.backward(b["q"], b["k"], b["v"], b["kd"], b["vd"], bf16_bits(dO), 0.3, nthreads=3)
+    k_lo = 30
+    ts = [0, 7, 19] + list(range(k_lo, T))
+    rows = np.array([t * Hq + h for t in ts for h in range(Hq)])
+    dq, dk, dv, dkd, dvd = orc.backward_rows(b["q"], b["k"], b["v"], b["kd"], b["vd"],
+                                             bf16_bits(dO), 0.3, rows, k_lo, nthreads=3)
+    assert np.allclose(dq, full[0].reshape(T * Hq, d)[rows], atol=1e-12)
+    assert np.allclose(dk, full[1][k_lo:], atol=1e-12) and np.allclose(dv, full[2][k_lo:], atol=1e-12)
+    G = Hq // Hk
+    for i, t in enumerate(ts):
+        for hk in range(Hk):
+            sel = slice(i * Hq + hk * G, i * Hq + (hk + 1) * G)
+            assert np.allclose(dkd[sel].sum(0), full[3][:, t, hk], atol=1e-12)
+            assert np.allclose(dvd[sel].sum(0), full[4][:, t, hk], atol=1e-12)
