@@ -48,7 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 def workload_by_name(name):
-    for w in [*wl.ALL, wl.LONG_L0]:
+    for w in [*wl.ALL, wl.LONG_L0, *wl.TABLE2]:
         if w.name == name:
             return w
     raise SystemExit(f"unknown workload {name}; known: {[w.name for w in wl.ALL]}")
@@ -251,6 +251,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="moda", choices=["moda", "reference"])
     ap.add_argument("--workload", default=wl.LONG.name)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=3,
+                    help="timed moda_bwd calls reported in the 'bwd' object (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=None,
                     help="seconds of oracle work for cpu_baseline (default 10) or per "
@@ -388,6 +390,37 @@ def main(argv=None):
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
+
+    # ---- backward (a separate measurement; not part of the forward step) ----
+    if args.bwd_steps > 0:
+        g = torch.Generator(device=dev)
+        g.manual_seed(1)
+        dO = torch.randn((w.T, w.Hq, w.d), generator=g, device=dev).to(torch.bfloat16)
+        f32 = dict(dtype=torch.float32, device=dev)
+        grads = (torch.empty((w.T, w.Hq, w.d), **f32), torch.empty((w.T, w.Hk, w.d), **f32),
+                 torch.empty((w.T, w.Hk, w.d), **f32),
+                 torch.empty((w.Hk, w.T, w.L, w.d), **f32) if w.L else None,
+                 torch.empty((w.Hk, w.T, w.L, w.d), **f32) if w.L else None)
+        delta = torch.empty((w.T, w.Hq), **f32)
+        moda.moda_fwd(q, k, v, kd if w.L else None, vd if w.L else None, w.scale, o=o, lse=lse,
+                      stream=stream)
+        bargs = (q, k, v, kd if w.L else None, vd if w.L else None, o, lse, dO, w.scale)
+        moda.moda_bwd(*bargs, grads=grads, delta=delta, stream=stream)
+        eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.bwd_steps)]
+        torch.cuda.synchronize(dev)
+        for a, b in eb:
+            a.record(stream)
+            moda.moda_bwd(*bargs, grads=grads, delta=delta, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        bwd_ms = statistics.median(a.elapsed_time(b) for a, b in eb)
+        Fb = 2.5 * F  # five GEMM-shaped products (S, dP, dV, dK, dQ) vs the forward's two
+        line["bwd"] = {"ms": bwd_ms, "tflops": Fb / (bwd_ms * 1e-3) / 1e12,
+                       "pct_peak_burst": 100 * Fb / (bwd_ms * 1e-3) / 1e12 / peak,
+                       "flops_counted": Fb, "fwd_plus_bwd_ms": fwd_ms + bwd_ms,
+                       "kernels": "delta + depth (CUDA cores) + dq + dk/dv (mma.sync)"}
+        del grads, delta, dO
 
     # ---- end to end: pinned host inputs in, o and lse out, every step ----
     if not args.no_e2e:

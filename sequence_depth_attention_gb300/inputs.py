@@ -67,6 +67,12 @@ LONG_L0 = LONG.with_L(0)
 
 ALL = [TINY, LAYER_700M, *GQA_SWEEP, *DEPTH_SWEEP, LONG]
 
+# The shape of the pages' kernel-efficiency table (Table 2: B=1, d=64, G=8,
+# Hq=64, Hk=8, L=64, T from 4K to 64K), for context runs of forward +
+# backward; not one of the five workloads above.
+TABLE2 = [Workload(f"table2-T{t}", T=t, Hq=64, Hk=8, d=64, L=64)
+          for t in (4096, 8192, 16384, 32768, 65536)]
+
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None):
     """Returns dict q[T,Hq,d], k[T,Hk,d], v[T,Hk,d], kd[L,T,Hk,d], vd[L,T,Hk,d] (bf16)."""
