@@ -135,6 +135,31 @@ MODA_API moda_status moda_bwd(const void* q, const void* k, const void* v, const
                               moda_stream_t stream);
 
 /*
+ * moda_bwd_noalloc -- moda_bwd without the caller's workspace; the paper has
+ * no counterpart. It is meant for callers that cannot give the library device
+ * memory for scratch: code whose device memory is owned by another allocator
+ * (a framework's caching allocator, a fixed pool sized up front) and code
+ * that must not risk cudaMalloc's implicit synchronisation. It allocates
+ * nothing: its scratch is a 4 MiB array compiled into the library, held by
+ * every GPU that loads it until the process exits.
+ *   Arguments and results as moda_bwd, minus `delta`.
+ *   Limit: T * Hq <= 1048576 (2^20) rows; larger calls return
+ *   MODA_ERR_UNSUPPORTED and launch nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ *   All calls share the one array, which keeps the last call's contents;
+ *   each call writes every element it reads, so nothing is cleared between
+ *   calls. Calls that overlap on the GPU (other streams, other host threads)
+ *   race on the array: serialise them.
+ */
+MODA_API moda_status moda_bwd_noalloc(const void* q, const void* k, const void* v,
+                                      const void* kd, const void* vd, const void* o,
+                                      const float* lse, const void* dO, int T, int Hq, int Hk,
+                                      int d, int L, float scale, float* dq, float* dk, float* dv,
+                                      float* dkd, float* dvd, moda_stream_t stream);
+
+/*
  * moda_get_device_error -- synchronises `stream`, then returns and clears
  * the current device's latched kernel error word (MODA_OK if none).
  */

@@ -24,7 +24,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_bwd", "moda_get_device_error",
+EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
@@ -59,6 +59,8 @@ def load():
         lib.moda_fwd.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
         lib.moda_bwd.restype = i
+        lib.moda_bwd_noalloc.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 6
+        lib.moda_bwd_noalloc.restype = i
         lib.moda_get_device_error.argtypes = [vp]
         lib.moda_get_device_error.restype = i
         lib.moda_selftest_wait_timeout.argtypes = [i, vp]
@@ -179,6 +181,23 @@ def moda_bwd(q, k, v, kd, vd, o, lse, dO, scale: float, grads=None, delta=None, 
                          _ptr(dvd if L else None), _ptr(delta), _stream(stream))
     _check(st, "moda_bwd")
     return dq, dk, dv, dkd, dvd
+
+
+def moda_bwd_noalloc(q, k, v, kd, vd, o, lse, dO, scale: float, grads, stream=None):
+    """moda_bwd on the library's fixed scratch (no workspace argument, nothing
+    allocated by either side). `grads` = (dq, dk, dv, dkd, dvd) fp32 tensors
+    the caller owns (dkd/dvd None when L == 0). T*Hq must be <= 2^20."""
+    T, Hq, d = q.shape
+    Hk = k.shape[1]
+    L = 0 if kd is None or kd.numel() == 0 else kd.shape[2]
+    dq, dk, dv, dkd, dvd = grads
+    st = load().moda_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kd if L else None),
+                                 _ptr(vd if L else None), _ptr(o), _ptr(lse), _ptr(dO), T, Hq, Hk,
+                                 d, L, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(dkd if L else None), _ptr(dvd if L else None),
+                                 _stream(stream))
+    _check(st, "moda_bwd_noalloc")
+    return grads
 
 
 def moda_get_device_error(stream=None) -> int:

@@ -76,6 +76,16 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 }  // namespace
 
+namespace moda {
+moda_status report(moda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return s;
+}
+}  // namespace moda
+
 extern "C" {
 
 const char* moda_status_string(moda_status s) {

@@ -38,6 +38,10 @@ struct BwdArgs {
 // Kernel error codes latched into the device error word (first one wins).
 enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 
+// Sets the calling thread's last-error detail (see moda_last_error_detail)
+// and returns s.
+moda_status report(moda_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+
 // Launchers. Return cudaSuccess or the launch error.
 cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
