@@ -391,6 +391,24 @@ def main(argv=None):
         "clocks": clk,
     }
 
+    # ---- layer-by-layer depth writes (the model path that replaces the pack) ----
+    if w.L:
+        layers_k = [kd_raw[l] for l in range(w.L)]
+        layers_v = [vd_raw[l] for l in range(w.L)]
+        for l in range(w.L):  # warm
+            moda.moda_depth_write(layers_k[l], kd, l, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for l in range(w.L):
+            moda.moda_depth_write(layers_k[l], kd, l, stream=stream)
+            moda.moda_depth_write(layers_v[l], vd, l, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        wms = a.elapsed_time(b)
+        line["depth_write"] = {"ms_all_layers_kd_and_vd": wms, "launches": 2 * w.L,
+                               "gbs": pack_bytes / (wms * 1e-3) / 1e9,
+                               "pct_hbm": 100 * pack_bytes / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
     # ---- backward (a separate measurement; not part of the forward step) ----
     if args.bwd_steps > 0:
         g = torch.Generator(device=dev)

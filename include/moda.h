@@ -69,6 +69,26 @@ MODA_API moda_status moda_pack_depth(const void* src, void* dst, int L, int T, i
                             int d, moda_stream_t stream);
 
 /*
+ * moda_depth_write -- write one layer's keys (or values) into slot `slot` of
+ * the packed depth stream as the layer runs (Sec. 2.2, "write": attention
+ * layers append their K, V; FFN layers the KV projection of their input):
+ *
+ *   dst[hk][t][slot][c] = src[t][hk][c]      (bit-exact copy)
+ *
+ *   src  [T, Hk, d] bf16, one layer's K or V
+ *   dst  [Hk, T, L, d] bf16, the packed stream moda_fwd reads; only slot
+ *        `slot` is written, 0 <= slot < L
+ * Writing every layer this way makes moda_pack_depth unnecessary.
+ * Bounded depth cache, sliding window (Sec. 6.2's fixed budget S << L): give
+ * the stream L = S slots and write layer l into slot l % S; moda_fwd with
+ * L = min(layers written, S) then attends to the most recent S slots (slot
+ * order does not matter to the joint softmax).
+ * Errors: INVALID_ARG, UNSUPPORTED (d, L > 1024), MISALIGNED, CUDA.
+ */
+MODA_API moda_status moda_depth_write(const void* src, void* dst, int T, int Hk, int d, int L,
+                                      int slot, moda_stream_t stream);
+
+/*
  * moda_fwd -- the MoDA forward (Sec. 2.2 joint softmax; Sec. 3.3 fused
  * kernel: group-aware query tiles, grouped causal mask, block-diagonal depth
  * mask, one online-softmax state).

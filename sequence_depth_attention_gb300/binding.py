@@ -24,7 +24,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_fwd", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
+EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_fwd", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
@@ -55,6 +55,8 @@ def load():
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.moda_pack_depth.argtypes = [vp, vp, i, i, i, i, vp]
         lib.moda_pack_depth.restype = i
+        lib.moda_depth_write.argtypes = [vp, vp, i, i, i, i, i, vp]
+        lib.moda_depth_write.restype = i
         lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
@@ -115,6 +117,19 @@ def moda_pack_depth(src: torch.Tensor, dst: torch.Tensor | None = None, stream=N
         raise ValueError(f"dst: expected shape {(Hk, T, L, d)}, got {tuple(dst.shape)}")
     st = load().moda_pack_depth(_ptr(src), _ptr(dst), L, T, Hk, d, _stream(stream))
     _check(st, "moda_pack_depth")
+    return dst
+
+
+def moda_depth_write(src: torch.Tensor, dst: torch.Tensor, slot: int, stream=None):
+    """Write one layer's K or V src[T,Hk,d] into slot `slot` of the packed
+    depth stream dst[Hk,T,L,d] (bit-exact). Returns dst."""
+    _need(src, "src"), _need(dst, "dst")
+    T, Hk, d = src.shape
+    if dst.dim() != 4 or dst.shape[0] != Hk or dst.shape[1] != T or dst.shape[3] != d:
+        raise ValueError(f"dst must be [Hk,T,L,d] with Hk={Hk}, T={T}, d={d}")
+    L = dst.shape[2]
+    st = load().moda_depth_write(_ptr(src), _ptr(dst), T, Hk, d, L, int(slot), _stream(stream))
+    _check(st, "moda_depth_write")
     return dst
 
 

@@ -1,0 +1,47 @@
+// Depth-stream write: one layer's K (or V) rows go straight into slot `slot`
+// of the packed depth stream, dst[hk][t][slot][:] = src[t][hk][:].
+//
+// Mixture-of-Depths Attention, Sec. 2.2 ("write" step): each attention layer
+// appends its K, V to the depth stream and each FFN layer the KV projection
+// of its input. Writing into the packed, per-position-contiguous layout as
+// the layers run removes the separate relayout of the whole stream.
+//
+// HBM-bound copy of 16-byte vectors: consecutive lanes walk the d/8 vectors
+// of one (t, hk) row, so reads are contiguous and each destination row of
+// d*2 bytes is written whole.
+#include "moda_internal.h"
+
+namespace moda {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+depth_write_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int T, int Hk, int L,
+                   int slot, int lg_vpr, int64_t total_vec) {
+  const int vpr = 1 << lg_vpr;
+  for (int64_t n = (int64_t)blockIdx.x * kThreads + threadIdx.x; n < total_vec;
+       n += (int64_t)gridDim.x * kThreads) {
+    const int c = (int)(n & (vpr - 1));
+    const int64_t row = n >> lg_vpr;  // t*Hk + hk
+    const int t = (int)(row / Hk);
+    const int hk = (int)(row - (int64_t)t * Hk);
+    dst[(((int64_t)hk * T + t) * L + slot) * vpr + c] = __ldg(src + n);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
+                               int num_sms, cudaStream_t stream) {
+  const int lg_vpr = d == 128 ? 4 : 3;
+  const int64_t total = (int64_t)T * Hk << lg_vpr;
+  int64_t blocks = (total + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  depth_write_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(
+      (const uint4*)src, (uint4*)dst, T, Hk, L, slot, lg_vpr, total);
+  return cudaGetLastError();
+}
+
+}  // namespace moda

@@ -124,6 +124,28 @@ moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk, in
   return ok();
 }
 
+moda_status moda_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
+                             moda_stream_t stream) {
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (Hk < 1) return fail(MODA_ERR_INVALID_ARG, "Hk = %d < 1", Hk);
+  if (L < 1) return fail(MODA_ERR_INVALID_ARG, "L = %d < 1", L);
+  if (slot < 0 || slot >= L) return fail(MODA_ERR_INVALID_ARG, "slot = %d outside [0, %d)", slot, L);
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if (!src || !dst) return fail(MODA_ERR_INVALID_ARG, "NULL src or dst");
+  if (!aligned16(src) || !aligned16(dst))
+    return fail(MODA_ERR_MISALIGNED, "src or dst not 16-byte aligned");
+  if (overlaps(src, (size_t)T * Hk * d * 2, dst, (size_t)Hk * T * L * d * 2))
+    return fail(MODA_ERR_INVALID_ARG, "src and dst overlap");
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_depth_write(src, dst, T, Hk, d, L, slot, sms, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "depth_write launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, int T, int Hq, int Hk, int d, int L, float scale, void* o,
                      float* lse, moda_stream_t stream) {

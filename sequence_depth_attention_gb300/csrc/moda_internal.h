@@ -48,6 +48,8 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
+                               int num_sms, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);
 
 }  // namespace moda

@@ -133,3 +133,14 @@ def test_product_package_does_not_import_oracle():
 @pytest.mark.parametrize("ms", [0, -1, 5001])
 def test_selftest_rejects_timeout(lib, ms):
     assert lib.moda_selftest_wait_timeout(ms, None) == INVALID
+
+
+@pytest.mark.parametrize("args,code", [
+    ((A, B, 0, 2, 64, 4, 0), INVALID), ((A, B, 8, 2, 64, 0, 0), INVALID),
+    ((A, B, 8, 2, 64, 4, 4), INVALID), ((A, B, 8, 2, 64, 4, -1), INVALID),
+    ((A, B, 8, 2, 96, 4, 0), UNSUPPORTED), ((A, B, 8, 2, 64, 2000, 0), UNSUPPORTED),
+    ((None, B, 8, 2, 64, 4, 0), INVALID), ((A + 8, B, 8, 2, 64, 4, 0), MISALIGNED),
+    ((A, A + 256, 8, 2, 64, 4, 0), INVALID),
+])
+def test_depth_write_rejects(lib, args, code):
+    assert lib.moda_depth_write(*args, None) == code
