@@ -251,6 +251,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="moda", choices=["moda", "reference"])
     ap.add_argument("--workload", default=wl.LONG.name)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=20,
+                    help="timed moda_decode calls reported in the 'decode' object (0 = skip)")
     ap.add_argument("--bwd-steps", type=int, default=3,
                     help="timed moda_bwd calls reported in the 'bwd' object (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -408,6 +410,39 @@ def main(argv=None):
         line["depth_write"] = {"ms_all_layers_kd_and_vd": wms, "launches": 2 * w.L,
                                "gbs": pack_bytes / (wms * 1e-3) / 1e9,
                                "pct_hbm": 100 * pack_bytes / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+    # ---- decode: the last position as a new token over the whole cache ----
+    if args.decode_steps > 0:
+        t = w.T - 1
+        qt = q[t].contiguous()
+        kt = kd[:, t] if w.L else None  # packed stream read in place
+        vt = vd[:, t] if w.L else None
+        ws = torch.empty((moda.moda_decode_workspace_bytes(w.T, w.Hq, w.d) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        od = torch.empty((w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+        ld = torch.empty((w.Hq,), dtype=torch.float32, device=dev)
+        # > L2; read (not written) before each call so L2 holds clean lines
+        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            moda.moda_decode(qt, k, v, kt, vt, w.scale, o=od, lse=ld, workspace=ws, stream=stream)
+        times = []
+        for _ in range(args.decode_steps):
+            sink = flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            moda.moda_decode(qt, k, v, kt, vt, w.scale, o=od, lse=ld, workspace=ws, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        dms = statistics.median(times)
+        dbytes = 2 * w.T * w.Hk * w.d * 2 + 2 * w.Hk * w.L * w.d * 2 + 2 * w.Hq * w.d * 2 + \
+            2 * ws.numel() * 4
+        line["decode"] = {"us_per_token": 1e3 * dms, "context": w.T, "bytes": dbytes,
+                          "gbs": dbytes / (dms * 1e-3) / 1e9,
+                          "pct_hbm": 100 * dbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "l2": "flushed (256 MB read) before every call",
+                          "launches_per_token": 2}
+        del flush, ws
 
     # ---- backward (a separate measurement; not part of the forward step) ----
     if args.bwd_steps > 0:

@@ -24,6 +24,7 @@
 #ifndef MODA_H_
 #define MODA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -121,6 +122,33 @@ MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
                      const void* kd, const void* vd, int T, int Hq, int Hk,
                      int d, int L, float scale, void* o, float* lse,
                      moda_stream_t stream);
+
+/*
+ * moda_decode -- one decoding step: the new token at position t = Tctx - 1
+ * attends, under one softmax, to the sequence KV cache (positions 0..t, its
+ * own K/V included) and to the L depth slots of position t (Sec. 2.2; the
+ * decode-time depth cache of Table 1 is these L slots of the current token).
+ * It is row t of moda_fwd for all Hq heads.
+ *
+ *   q            [Hq, d] bf16, the new token's queries
+ *   k_cache, v_cache  [Tctx, Hk, d] bf16
+ *   kd_tok, vd_tok    the L depth slots of position t: KV head hk's slots
+ *                form the [L, d] bf16 block at kd_tok + hk*depth_hk_stride
+ *                (elements). A standalone [Hk, L, d] tensor has stride L*d;
+ *                position t of the packed stream [Hk, T, L, d] has stride
+ *                T*L*d (pass &kd[0][t][0][0]). Stride >= L*d, multiple of 8.
+ *   o            [Hq, d] bf16 output; lse [Hq] fp32 (natural log) or NULL
+ *   workspace    caller-owned device scratch of at least
+ *                moda_decode_workspace_bytes(Tctx, Hq, d) bytes
+ * Memory-bound: every cache row is read once for the G heads of its KV head.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+MODA_API size_t moda_decode_workspace_bytes(int Tctx, int Hq, int d);
+MODA_API moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
+                                 const void* kd_tok, const void* vd_tok,
+                                 long long depth_hk_stride, int Tctx, int Hq, int Hk, int d,
+                                 int L, float scale, void* o, float* lse, float* workspace,
+                                 size_t workspace_bytes, moda_stream_t stream);
 
 /*
  * moda_bwd -- gradients of moda_fwd with respect to all of its inputs. The

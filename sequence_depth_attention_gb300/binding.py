@@ -24,7 +24,8 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_fwd", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
+EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_fwd", "moda_decode",
+           "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
@@ -57,6 +58,11 @@ def load():
         lib.moda_pack_depth.restype = i
         lib.moda_depth_write.argtypes = [vp, vp, i, i, i, i, i, vp]
         lib.moda_depth_write.restype = i
+        lib.moda_decode_workspace_bytes.argtypes = [i, i, i]
+        lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.moda_decode.argtypes = [vp] * 5 + [ctypes.c_longlong] + [i] * 5 + [f, vp, vp, vp,
+                                                                           ctypes.c_size_t, vp]
+        lib.moda_decode.restype = i
         lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
@@ -162,6 +168,46 @@ def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
     st = load().moda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L,
                          float(scale), _ptr(o), _ptr(lse), _stream(stream))
     _check(st, "moda_fwd")
+    return o, lse
+
+
+def moda_decode_workspace_bytes(Tctx: int, Hq: int, d: int) -> int:
+    return int(load().moda_decode_workspace_bytes(int(Tctx), int(Hq), int(d)))
+
+
+def moda_decode(q, k_cache, v_cache, kd_tok, vd_tok, scale: float, o=None, lse=None,
+                workspace=None, stream=None):
+    """One decoding step. q[Hq,d]; k_cache/v_cache[Tctx,Hk,d]; kd_tok/vd_tok
+    [Hk,L,d] views whose rows [L,d] are contiguous (stride(0) may be larger,
+    e.g. kd_packed[:, t]) or None when L == 0. Returns (o[Hq,d], lse[Hq])."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    Hq, d = q.shape
+    Tctx, Hk, _ = k_cache.shape
+    if kd_tok is None or kd_tok.numel() == 0:
+        L, stride = 0, 0
+        kd_tok = vd_tok = None
+    else:
+        L = kd_tok.shape[1]
+        for t, n in ((kd_tok, "kd_tok"), (vd_tok, "vd_tok")):
+            if not t.is_cuda or t.dtype != torch.bfloat16 or t.shape != (Hk, L, d) or \
+                    t.stride(2) != 1 or (L > 1 and t.stride(1) != d):
+                raise ValueError(f"{n}: expected a bf16 CUDA view [Hk,L,d] with contiguous [L,d] rows")
+        stride = kd_tok.stride(0) if Hk > 1 else L * d  # one head: the stride is never used
+        if Hk > 1 and kd_tok.stride(0) != vd_tok.stride(0):
+            raise ValueError("kd_tok and vd_tok must have the same KV-head stride")
+    if o is None:
+        o = torch.empty((Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq,), dtype=torch.float32, device=q.device)
+    need = moda_decode_workspace_bytes(Tctx, Hq, d)
+    if workspace is None:
+        workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=q.device)
+    st = load().moda_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kd_tok), _ptr(vd_tok),
+                            int(stride), Tctx, Hq, Hk, d, L, float(scale), _ptr(o), _ptr(lse),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream))
+    _check(st, "moda_decode")
     return o, lse
 
 

@@ -244,6 +244,66 @@ moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd
   return ok();
 }
 
+size_t moda_decode_workspace_bytes(int Tctx, int Hq, int d) {
+  if (Tctx < 1 || Hq < 1 || d < 1) return 0;
+  return (size_t)(moda::decode_num_splits(Tctx) + 1) * Hq * (d + 2) * sizeof(float);
+}
+
+moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const void* kd_tok, const void* vd_tok, long long depth_hk_stride,
+                        int Tctx, int Hq, int Hk, int d, int L, float scale, void* o, float* lse,
+                        float* workspace, size_t workspace_bytes, moda_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !o || !workspace)
+    return fail(MODA_ERR_INVALID_ARG, "NULL q, cache, o or workspace");
+  if (Tctx < 1) return fail(MODA_ERR_INVALID_ARG, "Tctx = %d < 1", Tctx);
+  if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
+  if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
+  if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
+  if (L > 0 && (!kd_tok || !vd_tok)) return fail(MODA_ERR_INVALID_ARG, "NULL depth slots with L = %d", L);
+  if (!(scale > 0.f) || scale == __builtin_inff())
+    return fail(MODA_ERR_INVALID_ARG, "scale must be positive and finite");
+  const int G = Hq / Hk;
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
+  if (Tctx > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "Tctx = %d > 2^24", Tctx);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if (L > 0 && (depth_hk_stride < (long long)L * d || depth_hk_stride % 8 != 0))
+    return fail(MODA_ERR_INVALID_ARG, "depth_hk_stride = %lld must be >= L*d and a multiple of 8",
+                depth_hk_stride);
+  if (workspace_bytes < moda_decode_workspace_bytes(Tctx, Hq, d))
+    return fail(MODA_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                moda_decode_workspace_bytes(Tctx, Hq, d));
+  const void* al[] = {q, k_cache, v_cache, o, workspace, lse, L ? kd_tok : nullptr, L ? vd_tok : nullptr};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return fail(MODA_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  const size_t qb = (size_t)Hq * d * 2, cb = (size_t)Tctx * Hk * d * 2;
+  const size_t db = L ? ((size_t)(Hk - 1) * depth_hk_stride + (size_t)L * d) * 2 : 0;
+  const void* ins[] = {q, k_cache, v_cache, L ? kd_tok : nullptr, L ? vd_tok : nullptr};
+  const size_t insz[] = {qb, cb, cb, db, db};
+  void* outs[] = {o, lse, workspace};
+  const size_t outsz[] = {qb, lse ? (size_t)Hq * 4 : 0, workspace_bytes};
+  for (int a = 0; a < 3; ++a) {
+    for (int b = 0; b < 5; ++b)
+      if (overlaps(outs[a], outsz[a], ins[b], insz[b]))
+        return fail(MODA_ERR_INVALID_ARG, "an output or the workspace overlaps an input");
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(outs[a], outsz[a], outs[b], outsz[b]))
+        return fail(MODA_ERR_INVALID_ARG, "outputs overlap");
+  }
+  moda::DecodeArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.kd = L ? kd_tok : nullptr; a.vd = L ? vd_tok : nullptr;
+  a.depth_hk_stride = depth_hk_stride;
+  a.Tctx = Tctx; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G; a.scale = scale;
+  a.o = o; a.lse = lse; a.work = workspace;
+  int dev;
+  moda_status st = device_state(&dev, &a.err, &a.num_sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_decode(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 moda_status moda_selftest_wait_timeout(int timeout_ms, moda_stream_t stream) {
   if (timeout_ms < 1 || timeout_ms > 5000)
     return fail(MODA_ERR_INVALID_ARG, "timeout_ms = %d (allowed 1..5000)", timeout_ms);

@@ -35,6 +35,20 @@ struct BwdArgs {
   float* delta;                              // [T, Hq] caller workspace
 };
 
+// Arguments of one decode call after validation on the host.
+struct DecodeArgs {
+  const void *q, *k, *v, *kd, *vd;  // q [Hq,d]; k/v cache [Tctx,Hk,d]; depth slots (see stride)
+  int64_t depth_hk_stride;           // elements between the [L,d] blocks of consecutive KV heads
+  int Tctx, Hq, Hk, d, L, G;
+  float scale;
+  void* o;                           // [Hq,d] bf16
+  float* lse;                        // [Hq] or nullptr
+  float* work;                       // partials, decode_workspace_floats
+  unsigned int* err;                 // device error word
+  int num_sms;
+};
+int decode_num_splits(int Tctx);
+
 // Kernel error codes latched into the device error word (first one wins).
 enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 
@@ -48,6 +62,7 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
                                int num_sms, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);

@@ -14,4 +14,9 @@ namespace moda {
 CUresult encode_bf16_sw128(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides_bytes, const uint32_t* box);
 
+// Same, without swizzle: boxes land in shared memory as plain row-major
+// arrays (the inner box extent must be a multiple of 16 bytes).
+CUresult encode_bf16_plain(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box);
+
 }  // namespace moda

@@ -144,3 +144,30 @@ def test_selftest_rejects_timeout(lib, ms):
 ])
 def test_depth_write_rejects(lib, args, code):
     assert lib.moda_depth_write(*args, None) == code
+
+
+def test_decode_workspace_formula(lib):
+    lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
+    # (splits + 1) partials of (d + 2) floats per head; splits <= ceil(T/64), capped at 128
+    assert lib.moda_decode_workspace_bytes(1, 16, 128) == 2 * 16 * 130 * 4
+    assert lib.moda_decode_workspace_bytes(640, 16, 128) == 11 * 16 * 130 * 4
+    assert lib.moda_decode_workspace_bytes(65536, 16, 128) == 129 * 16 * 130 * 4
+    assert lib.moda_decode_workspace_bytes(0, 16, 128) == 0
+
+
+def _dec(lib, q=A, kc=B, vc=C, kt=D, vt=E, stride=4 * 64, T=100, Hq=4, Hk=2, d=64, L=4,
+         scale=0.125, o=O, lse=LSE, ws=0x78000000, wsb=1 << 20):
+    lib.moda_decode.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_longlong] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p]
+    return lib.moda_decode(q, kc, vc, kt, vt, stride, T, Hq, Hk, d, L, scale, o, lse, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(ws=None), INVALID), (dict(T=0), INVALID),
+    (dict(kt=None), INVALID), (dict(stride=4 * 64 - 8), INVALID), (dict(stride=4 * 64 + 3), INVALID),
+    (dict(wsb=16), INVALID), (dict(d=96), UNSUPPORTED), (dict(Hq=6, Hk=2), UNSUPPORTED),
+    (dict(q=A + 2), MISALIGNED), (dict(o=B), INVALID), (dict(scale=-1.0), INVALID),
+])
+def test_decode_rejects(lib, kw, code):
+    assert _dec(lib, **kw) == code
