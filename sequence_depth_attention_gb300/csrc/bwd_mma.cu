@@ -94,7 +94,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
                  int Hk, int L, float scale_log2, float scale, float* __restrict__ dq,
                  float* __restrict__ dkd, float* __restrict__ dvd) {
   constexpr int E = D / 32;  // columns per lane in phase 2
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DepthWarpSmem<D, G>& sm = reinterpret_cast<DepthWarpSmem<D, G>*>(smem_raw)[warp];
   const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
@@ -548,19 +548,8 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t st) {
     }
     if (e != cudaSuccess) return e;
   }
-  {
-    const int P = BM >> lgG;
-    const int ntiles = (a.T + P - 1) / P;
-    const size_t smem = (size_t)(2 * BM + 4 * BN) * D * sizeof(__nv_bfloat16);
-    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<(unsigned)((int64_t)ntiles * a.Hk), kThreads, smem, st>>>(
-        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-        (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, lgG, ntiles,
-        a.scale * kLog2e, a.scale, a.dq, a.L > 0 ? 1 : 0);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_bwd_dq_tc(a, st);
+  if (e != cudaSuccess) return e;
   {
     const int nk = (a.T + BM - 1) / BM;
     const size_t smem = (size_t)(2 * BM + 4 * BN) * D * sizeof(__nv_bfloat16) + 4 * BN * sizeof(float);
@@ -575,7 +564,27 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t st) {
   return e;
 }
 
+template <int D>
+cudaError_t launch_dq_mma(const BwdArgs& a, cudaStream_t st) {
+  const int lgG = __builtin_ctz((unsigned)a.G);
+  const int P = BM >> lgG;
+  const int ntiles = (a.T + P - 1) / P;
+  const size_t smem = (size_t)(2 * BM + 4 * BN) * D * sizeof(__nv_bfloat16);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<D><<<(unsigned)((int64_t)ntiles * a.Hk), kThreads, smem, st>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, lgG, ntiles,
+      a.scale * kLog2e, a.scale, a.dq, a.L > 0 ? 1 : 0);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_dq_mma<128>(a, stream) : launch_dq_mma<64>(a, stream);
+}
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
   return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);

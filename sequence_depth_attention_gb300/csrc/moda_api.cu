@@ -235,9 +235,8 @@ moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd
   a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G; a.scale = scale;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dkd = L ? dkd : nullptr; a.dvd = L ? dvd : nullptr;
   a.delta = delta;
-  int dev, sms;
-  unsigned int* err;
-  moda_status st = device_state(&dev, &err, &sms);
+  int dev;
+  moda_status st = device_state(&dev, &a.err, &a.num_sms);
   if (st != MODA_OK) return st;
   cudaError_t e = moda::launch_bwd(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_bwd launch: %s", cudaGetErrorString(e));

@@ -33,6 +33,8 @@ struct BwdArgs {
   float scale;
   float *dq, *dk, *dv, *dkd, *dvd;           // fp32 outputs (dkd/dvd packed)
   float* delta;                              // [T, Hq] caller workspace
+  unsigned int* err;                         // device error word of the current device
+  int num_sms;
 };
 
 // Arguments of one decode call after validation on the host.
@@ -62,6 +64,10 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// The sequence share of dq, added to what the depth kernel wrote (L > 0) or
+// written (L == 0): tcgen05 version (dispatched) and mma.sync version.
+cudaError_t launch_bwd_dq_tc(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
                                int num_sms, cudaStream_t stream);
