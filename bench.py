@@ -472,7 +472,7 @@ def main(argv=None):
         line["bwd"] = {"ms": bwd_ms, "tflops": Fb / (bwd_ms * 1e-3) / 1e12,
                        "pct_peak_burst": 100 * Fb / (bwd_ms * 1e-3) / 1e12 / peak,
                        "flops_counted": Fb, "fwd_plus_bwd_ms": fwd_ms + bwd_ms,
-                       "kernels": "delta + depth (CUDA cores) + dq (tcgen05) + dk/dv (mma.sync)"}
+                       "kernels": "delta + depth (CUDA cores) + dq + dk/dv (tcgen05)"}
         del grads, delta, dO
 
     # ---- end to end: pinned host inputs in, o and lse out, every step ----

@@ -1,0 +1,392 @@
+// dK and dV of the MoDA backward on the 5th-generation tensor core (sm_103a).
+//
+// One CTA owns a block of 128 keys of one KV head (K and V stay in shared
+// memory) and walks over the query rows that can see it in sub-tiles of 64
+// G-stacked rows (64/G positions x G heads, one 3-D TMA box as in the
+// forward). For each sub-tile c:
+//   S^T_c  = K Q_c^T,  dP^T_c = V dO_c^T             (tcgen05, 128 x 64 into TMEM)
+//   P^T_c  = exp2(S^T_c scale log2e - lse log2e)      (per column: the query's lse)
+//   dS^T_c = P^T_c * (dP^T_c - D)                     (CUDA cores, lane = key)
+//   dV += P^T_c dO_c,  dK += dS^T_c Q_c               (tcgen05, A from TMEM,
+//                                                      Q_c / dO_c read MN-major)
+// Only the sequence keys are handled here; the depth slots' gradients come
+// from the depth kernel. dk is written times the softmax scale.
+//
+// Roles (12 warps): warp 0 TMA (K, V once, then the Q/dO ring); warp 1 issues
+// MMAs; warps 4-7 and 8-11 each take 32 of the 64 columns for all 128 keys.
+// TMEM columns: S^T [0,64), dP^T [64,128), two P^T|dS^T buffers [128,192)
+// [192,256) (per column half: 16 columns of P^T then 16 of dS^T, bf16 pairs),
+// dV [256,256+d), dK [256+d,256+2d).
+// Issue order: S_0 dP_0, then per c: S_{c+1} dP_{c+1} once the softmax holds
+// S_c and dP_c in registers, then dV_c dK_c once P^T_c and dS^T_c are stored.
+// All waits are bounded; on expiry the CTA drains and latches MODA_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+
+#include "moda_internal.h"
+#include "sm103.cuh"
+#include "tensor_map.h"
+
+namespace moda {
+namespace {
+
+using namespace sm103;
+
+constexpr int BK = 128;  // keys per CTA
+constexpr int BQ = 64;   // G-stacked query rows per sub-tile
+constexpr int kThreads = 384;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct KvCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kKBox = BK * 128;  // bytes of one 64-column box of K or V
+  static constexpr int kQBox = BQ * 128;  // bytes of one 64-column box of a Q or dO sub-tile
+  static constexpr int kKTile = kBoxes * kKBox;
+  static constexpr int kQTile = kBoxes * kQBox;
+  static constexpr int kNS = D == 128 ? 4 : 6;  // Q/dO ring stages
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKTile;
+  static constexpr int kOffQ = kOffV + kKTile;           // stage s: Q at kOffQ + s*2*kQTile
+  static constexpr int kOffRow = kOffQ + kNS * 2 * kQTile;  // per-warp lse2 / D staging
+  static constexpr int kOffBar = kOffRow + 8 * 2 * 32 * 4;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kColS = 0, kColP = 64, kColB = 128, kColV = 256, kColK = 256 + D;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct alignas(8) KvBars {
+  uint64_t kv_full;
+  uint64_t q_full[6], q_empty[6];
+  uint64_t s_full, s_free;
+  uint64_t pd_full[2], pd_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(KvBars) <= 256, "barrier block");
+
+struct KvParams {
+  int T, Hq, Hk, lgG;
+  float scale_log2, scale;
+  const float* lse;
+  const float* delta;
+  float* dk;
+  float* dv;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const KvParams p) {
+  using C = KvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  KvBars* bars = reinterpret_cast<KvBars*>(smem + C::kOffBar);
+  const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = 1 << p.lgG;
+  const int PQ = BQ >> p.lgG;  // positions per sub-tile
+  const int kb = (int)(blockIdx.x / p.Hk);  // longest first: early keys see the most queries
+  const int hk = (int)(blockIdx.x % p.Hk);
+  const int q0 = kb * BK;                   // first query position that sees this block
+  const int n = (p.T - q0 + PQ - 1) / PQ;   // sub-tiles
+
+  if (tid == 0) {
+    bars->abort = 0;
+    mbar_init(smem_u32(&bars->kv_full), 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 1);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->s_free), 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->pd_full[b]), 256);
+      mbar_init(smem_u32(&bars->pd_done[b]), 1);
+    }
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    const bool leader = elect_one();
+    if (leader) {
+      const uint32_t kvb = smem_u32(&bars->kv_full);
+      mbar_arrive_expect_tx(kvb, 2 * C::kKTile);
+      for (int c = 0; c < C::kBoxes; ++c) {
+        tma_load_3d(sK + c * C::kKBox, &tmK, kvb, c * 64, hk, q0);
+        tma_load_3d(sV + c * C::kKBox, &tmV, kvb, c * 64, hk, q0);
+      }
+    }
+    int issued = 0;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % C::kNS;
+      if (!warp_wait(smem_u32(&bars->q_empty[s]), ((i / C::kNS) & 1) ^ 1, abort)) break;
+      if (leader) {
+        const uint32_t fb = smem_u32(&bars->q_full[s]);
+        const uint32_t dst = sQ + s * 2 * C::kQTile;
+        mbar_arrive_expect_tx(fb, 2 * C::kQTile);
+        for (int c = 0; c < C::kBoxes; ++c) {
+          tma_load_3d(dst + c * C::kQBox, &tmQ, fb, c * 64, hk * G, q0 + i * PQ);
+          tma_load_3d(dst + C::kQTile + c * C::kQBox, &tmO, fb, c * 64, hk * G, q0 + i * PQ);
+        }
+      }
+      __syncwarp();
+      issued = i + 1;
+    }
+    if (leader) {
+      int never = 0;
+      for (int i = max(0, issued - C::kNS); i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&bars->q_full[i % C::kNS]), (i / C::kNS) & 1, &never, kTimeoutNs);
+      mbar_wait_bounded(smem_u32(&bars->kv_full), 0, &never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, false);  // S^T, dP^T: K-major A and B
+    constexpr uint32_t idG = idesc_bf16_f32(BK, D, true);    // dV, dK: B read MN-major
+    const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dqmn = sdesc_sw128(sQ, C::kQBox, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+      return __all_sync(0xffffffffu, ok);
+    };
+    auto issue_sdp = [&](int i) {  // S^T_i and dP^T_i
+      const uint32_t stage = (uint32_t)((i % C::kNS) * 2 * C::kQTile) >> 4;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
+          const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
+          mma_ss(tbase + C::kColS, dk_ + ka, dq_ + stage + qa, idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
+          const uint32_t qa = ((C::kQTile + (kk >> 2) * C::kQBox + (kk & 3) * 32)) >> 4;
+          mma_ss(tbase + C::kColP, dv_ + ka, dq_ + stage + qa, idS, kk > 0);
+        }
+        tc_commit(smem_u32(&bars->s_full));
+      }
+      __syncwarp();
+    };
+    auto issue_grad = [&](int i) {  // dV += P^T_i dO_i, dK += dS^T_i Q_i; frees stage and buffer
+      const int s = i % C::kNS, b = i & 1;
+      const uint32_t stage = (uint32_t)(s * 2 * C::kQTile) >> 4;
+      if (leader) {
+        const uint32_t abuf = tbase + C::kColB + b * 64;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t acol = abuf + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
+          mma_ts(tbase + C::kColV, acol, dqmn + stage + (C::kQTile >> 4) + boff, idG,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::kColK, acol + 16, dqmn + stage + boff, idG, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&bars->q_empty[s]));
+        tc_commit(smem_u32(&bars->pd_done[b]));
+      }
+      __syncwarp();
+    };
+    bool ok = wait(&bars->kv_full, 0) && wait(&bars->q_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      issue_sdp(0);
+    }
+    for (int i = 0; ok && i < n; ++i) {
+      if (i + 1 < n) {
+        if (!wait(&bars->s_free, i & 1)) break;
+        if (!wait(&bars->q_full[(i + 1) % C::kNS], ((i + 1) / C::kNS) & 1)) break;
+        tc_fence_after();
+        issue_sdp(i + 1);
+      }
+      if (!wait(&bars->pd_full[i & 1], (i >> 1) & 1)) break;
+      tc_fence_after();
+      issue_grad(i);
+    }
+    if (leader) {
+      int never = 0;
+      tc_commit(smem_u32(&bars->mma_done));
+      mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ P^T and dS^T (two column halves)
+    const int half = (warp - 4) >> 2, q4 = warp & 3;
+    const int row = q4 * 32 + lane;  // key within the block
+    const uint32_t lane_base = (uint32_t)q4 * 32;
+    const int key = q0 + row;
+    float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64;
+    const float sl = p.scale_log2;
+    const int col = half * 32 + lane;  // the column this lane fetches lse and D for
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int t0 = q0 + i * PQ;
+      {
+        const int t = t0 + (col >> p.lgG);
+        const int64_t ri = (int64_t)t * p.Hq + hk * G + (col & (G - 1));
+        const bool valid = t < p.T;
+        const float l2 = valid ? __ldg(p.lse + ri) * kLog2e : INFINITY;
+        const float dd = valid ? __ldg(p.delta + ri) : 0.f;
+        __syncwarp();
+        rowbuf[lane] = l2;
+        rowbuf[32 + lane] = dd;
+        __syncwarp();
+      }
+      if (!warp_wait(smem_u32(&bars->s_full), i & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[32], y[32];
+      tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + half * 32), x);
+      tmem_ld32(tmem_addr(tbase, lane_base, C::kColP + half * 32), y);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->s_free));
+      // causal: column c (position t0 + c/G) sees this key iff key <= position
+      const int cmin = (key - t0) * G;  // first visible column of the sub-tile
+      const int first = cmin - half * 32;    // first visible local column of this half
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(rowbuf + c);
+        const float4 d4 = *reinterpret_cast<const float4*>(rowbuf + 32 + c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pp[4], ds[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pe = ex2_approx(fmaf(__uint_as_float(x[c + e]), sl, -lv[e]));
+          const bool vis = c + e >= first;
+          pp[e] = vis ? pe : 0.f;
+          ds[e] = vis ? pe * (__uint_as_float(y[c + e]) - dv[e]) : 0.f;
+        }
+        pk[c / 2] = pack_bf16x2(pp[0], pp[1]);
+        pk[c / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+        pk[16 + c / 2] = pack_bf16x2(ds[0], ds[1]);
+        pk[16 + c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+      // buffer i&1 last held sub-tile i-2: the tensor core must have consumed it
+      if (i >= 2) {
+        if (!warp_wait(smem_u32(&bars->pd_done[i & 1]), ((i - 2) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tmem_addr(tbase, lane_base, C::kColB + (i & 1) * 64 + half * 32), pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->pd_full[i & 1]));
+    }
+    if (ok) {
+      ok = warp_wait(smem_u32(&bars->pd_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, abort);
+      if (ok && n >= 2)
+        ok = warp_wait(smem_u32(&bars->pd_done[(n - 2) & 1]), ((n - 2) >> 1) & 1, abort);
+    }
+    if (ok) {
+      tc_fence_after();
+      // half 0 writes dV, half 1 writes dK (times the softmax scale)
+      const uint32_t c0 = half ? C::kColK : C::kColV;
+      const float mul = half ? p.scale : 1.f;
+      float* out = (half ? p.dk : p.dv) + ((int64_t)key * p.Hk + hk) * D;
+      const bool valid = key < p.T;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, c0 + c * 32), r);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(out + c * 32 + e) =
+                make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
+                            __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+  if (tid == 0 && bars->abort) atomicCAS(p.err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = KvCfg<D>;
+  const int lgG = __builtin_ctz((unsigned)a.G);
+  const int PQ = BQ >> lgG;
+  const int nk = (a.T + BK - 1) / BK;
+  CUtensorMap tq, to, tk, tv;
+  const uint64_t row = (uint64_t)D * 2;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hq};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)PQ};
+    if (encode_bf16_sw128(&tq, a.q, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&to, a.dO, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hk};
+    const uint32_t box[3] = {64, 1, BK};
+    if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  KvParams prm;
+  prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.lgG = lgG;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.scale = a.scale;
+  prm.lse = a.lse;
+  prm.delta = a.delta;
+  prm.dk = a.dk;
+  prm.dv = a.dv;
+  prm.err = a.err;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_tc_kernel<D><<<(unsigned)((int64_t)nk * a.Hk), kThreads, C::kSmemBytes, stream>>>(
+      tq, to, tk, tv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dkdv_tc(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
+}
+
+}  // namespace moda

@@ -550,18 +550,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t st) {
   }
   e = launch_bwd_dq_tc(a, st);
   if (e != cudaSuccess) return e;
-  {
-    const int nk = (a.T + BM - 1) / BM;
-    const size_t smem = (size_t)(2 * BM + 4 * BN) * D * sizeof(__nv_bfloat16) + 4 * BN * sizeof(float);
-    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    bwd_dkdv_kernel<D><<<(unsigned)((int64_t)nk * a.Hk), kThreads, smem, st>>>(
-        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-        (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, lgG, a.scale * kLog2e,
-        a.scale, a.dk, a.dv);
-    e = cudaGetLastError();
-  }
-  return e;
+  return launch_bwd_dkdv_tc(a, st);
 }
 
 template <int D>
@@ -580,7 +569,26 @@ cudaError_t launch_dq_mma(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_dkdv_mma(const BwdArgs& a, cudaStream_t st) {
+  const int lgG = __builtin_ctz((unsigned)a.G);
+  const int nk = (a.T + BM - 1) / BM;
+  const size_t smem = (size_t)(2 * BM + 4 * BN) * D * sizeof(__nv_bfloat16) + 4 * BN * sizeof(float);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<D><<<(unsigned)((int64_t)nk * a.Hk), kThreads, smem, st>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, lgG, a.scale * kLog2e,
+      a.scale, a.dk, a.dv);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_dkdv_mma(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_dkdv_mma<128>(a, stream) : launch_dkdv_mma<64>(a, stream);
+}
 
 cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream) {
   return a.d == 128 ? launch_dq_mma<128>(a, stream) : launch_dq_mma<64>(a, stream);

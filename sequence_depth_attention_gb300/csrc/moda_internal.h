@@ -68,6 +68,9 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // written (L == 0): tcgen05 version (dispatched) and mma.sync version.
 cudaError_t launch_bwd_dq_tc(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream);
+// dk and dv of the sequence keys: tcgen05 version (dispatched) and mma.sync version.
+cudaError_t launch_bwd_dkdv_tc(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_mma(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
                                int num_sms, cudaStream_t stream);
