@@ -81,6 +81,39 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// For 32 columns of one key row: P^T = exp2(S^T scale log2e - lse log2e) and
+// dS^T = P^T (dP^T - D), packed to bf16 pairs (P^T in pk[0,16), dS^T in
+// pk[16,32)). nrow holds -lse log2e in [0,32) and -D in [32,64) per column.
+// Columns below `first` are zero when kMask.
+template <bool kMask>
+__device__ __forceinline__ void pds_pack(const uint32_t* x, const uint32_t* y, const float* nrow,
+                                         uint64_t sl2, int first, uint32_t* pk) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(nrow + c);
+    const float4 d4 = *reinterpret_cast<const float4*>(nrow + 32 + c);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = c + 2 * h;
+      const uint64_t nl = h ? f2(l4.z, l4.w) : f2(l4.x, l4.y);
+      const uint64_t nd = h ? f2(d4.z, d4.w) : f2(d4.x, d4.y);
+      float a0, a1, s0, s1;
+      f2_split(ffma2(f2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sl2, nl), a0, a1);
+      float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+      const uint64_t dd = fadd2(f2(__uint_as_float(y[e]), __uint_as_float(y[e + 1])), nd);
+      f2_split(fmul2(f2(p0, p1), dd), s0, s1);
+      if (kMask) {
+        p0 = e >= first ? p0 : 0.f;
+        p1 = e + 1 >= first ? p1 : 0.f;
+        s0 = e >= first ? s0 : 0.f;
+        s1 = e + 1 >= first ? s1 : 0.f;
+      }
+      pk[e / 2] = pack_bf16x2(p0, p1);
+      pk[16 + e / 2] = pack_bf16x2(s0, s1);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
@@ -245,7 +278,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t lane_base = (uint32_t)q4 * 32;
     const int key = q0 + row;
     float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64;
-    const float sl = p.scale_log2;
+    const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
     const int col = half * 32 + lane;  // the column this lane fetches lse and D for
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
@@ -254,8 +287,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int t = t0 + (col >> p.lgG);
         const int64_t ri = (int64_t)t * p.Hq + hk * G + (col & (G - 1));
         const bool valid = t < p.T;
-        const float l2 = valid ? __ldg(p.lse + ri) * kLog2e : INFINITY;
-        const float dd = valid ? __ldg(p.delta + ri) : 0.f;
+        const float l2 = valid ? -__ldg(p.lse + ri) * kLog2e : -INFINITY;
+        const float dd = valid ? -__ldg(p.delta + ri) : 0.f;
         __syncwarp();
         rowbuf[lane] = l2;
         rowbuf[32 + lane] = dd;
@@ -272,27 +305,14 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->s_free));
-      // causal: column c (position t0 + c/G) sees this key iff key <= position
-      const int cmin = (key - t0) * G;  // first visible column of the sub-tile
-      const int first = cmin - half * 32;    // first visible local column of this half
+      // causal: column c (position t0 + c/G) sees this key iff key <= position;
+      // sub-tiles at or after the block's last key need no mask
       uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(rowbuf + c);
-        const float4 d4 = *reinterpret_cast<const float4*>(rowbuf + 32 + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pp[4], ds[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pe = ex2_approx(fmaf(__uint_as_float(x[c + e]), sl, -lv[e]));
-          const bool vis = c + e >= first;
-          pp[e] = vis ? pe : 0.f;
-          ds[e] = vis ? pe * (__uint_as_float(y[c + e]) - dv[e]) : 0.f;
-        }
-        pk[c / 2] = pack_bf16x2(pp[0], pp[1]);
-        pk[c / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-        pk[16 + c / 2] = pack_bf16x2(ds[0], ds[1]);
-        pk[16 + c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+      if (t0 < q0 + BK - 1) {
+        const int first = (key - t0) * G - half * 32;  // first visible local column
+        pds_pack<true>(x, y, rowbuf, sl2, first, pk);
+      } else {
+        pds_pack<false>(x, y, rowbuf, sl2, 0, pk);
       }
       // buffer i&1 last held sub-tile i-2: the tensor core must have consumed it
       if (i >= 2) {

@@ -76,6 +76,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// dS = exp2(S scale log2e - lse log2e) (dP - D) for 64 columns of one row,
+// packed to bf16 pairs; columns >= span are zero when kMask.
+template <bool kMask>
+__device__ __forceinline__ void ds_pack(const uint32_t* x, const uint32_t* y, uint64_t sl2,
+                                        uint64_t nl2, uint64_t nD2, int span, uint32_t* pk) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float a0, a1, d0, d1;
+    f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nl2), a0, a1);
+    const uint64_t dd = fadd2(f2(__uint_as_float(y[2 * c]), __uint_as_float(y[2 * c + 1])), nD2);
+    f2_split(fmul2(f2(ex2_approx(a0), ex2_approx(a1)), dd), d0, d1);
+    if (kMask) {
+      d0 = 2 * c < span ? d0 : 0.f;
+      d1 = 2 * c + 1 < span ? d1 : 0.f;
+    }
+    pk[c] = pack_bf16x2(d0, d1);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
@@ -258,7 +277,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float lse2 = valid ? p.lse[ri] * kLog2e : INFINITY;
     const float Dr = valid ? p.delta[ri] : 0.f;
     const int t_mask = min(t_row, p.T - 1);
-    const float sl = p.scale_log2;
+    const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(-lse2, -lse2), nD2 = f2(-Dr, -Dr);
     bool ok = true;
     for (int j = 0; j < nb && ok; ++j) {
       if (!warp_wait(smem_u32(&bars->s_full), j & 1, abort)) {
@@ -274,19 +293,14 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->s_free));
-      // causal mask (key <= t_row) on blocks that reach past p0
+      // causal mask (key <= t_row), needed only on the blocks that reach past p0
       const int k0 = j * BN + half * 64;
-      const int span = (k0 + 63 > p0) ? max(0, min(64, t_mask - k0 + 1)) : 64;
       uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float d0 = ex2_approx(fmaf(__uint_as_float(x[2 * c]), sl, -lse2)) *
-                   (__uint_as_float(y[2 * c]) - Dr);
-        float d1 = ex2_approx(fmaf(__uint_as_float(x[2 * c + 1]), sl, -lse2)) *
-                   (__uint_as_float(y[2 * c + 1]) - Dr);
-        d0 = 2 * c < span ? d0 : 0.f;
-        d1 = 2 * c + 1 < span ? d1 : 0.f;
-        pk[c] = pack_bf16x2(d0, d1);
+      if (j * BN + BN - 1 > p0) {
+        const int span = max(0, min(64, t_mask - k0 + 1));
+        ds_pack<true>(x, y, sl2, nl2, nD2, span, pk);
+      } else {
+        ds_pack<false>(x, y, sl2, nl2, nD2, 64, pk);
       }
       // dS_j reuses the buffer of dS_{j-2}: the tensor core must have consumed it
       if (j >= 2) {
