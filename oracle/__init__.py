@@ -19,8 +19,13 @@ Sec. 2.2 "MoDA"):
 Inputs are bf16 bit patterns as ``numpy.uint16`` arrays in the layouts
 q[T,Hq,d], k/v[T,Hk,d] and the UNPACKED depth stream kd/vd[L,T,Hk,d].
 
+``Oracle.kv_proj`` is the depth K/V of an FFN layer, a linear map of the
+FFN's input (reading notes Sec. 二.3; summary Sec. 2.2, the "write" step):
+out[t, n] = sum_c x[t, c] * w[n, c] in fp64.
+
 Pins (what ties this oracle to the pages and the mathematics rather than to
-itself) are in ``tests/test_oracle_pins.py``; every function here is pinned.
+itself) are in ``tests/test_oracle_pins.py``, ``tests/test_oracle_bwd.py`` and
+``tests/test_oracle_kvproj.py``; every function here is pinned.
 """
 from __future__ import annotations
 
@@ -101,6 +106,8 @@ class Oracle:
         lib.moda_oracle_bwd_rows.argtypes = [u16p] * 6 + [i] * 5 + [ctypes.c_double, i64p,
                                               ctypes.c_int64, i] + [f64p] * 5 + [i]
         lib.moda_oracle_bwd_rows.restype = ctypes.c_int
+        lib.moda_oracle_kv_proj.argtypes = [u16p, u16p, i, i, i, i64p, ctypes.c_int64, f64p]
+        lib.moda_oracle_kv_proj.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -200,6 +207,27 @@ class Oracle:
         return dq, dk, dv, dkd, dvd
 
 
+    def kv_proj(self, x, w, rows=None):
+        """Linear depth-KV projection of an FFN layer's input: x [T,Dm] and
+        w [N,Dm] (bf16 bits, one weight row per output feature). Returns
+        float64 out [len(rows), N] (all T rows when rows is None), unrounded."""
+        x, w = _u16(x, "x"), _u16(w, "w")
+        if x.ndim != 2 or w.ndim != 2 or x.shape[1] != w.shape[1]:
+            raise ValueError("x must be [T,Dm] and w [N,Dm]")
+        T, Dm = x.shape
+        N = w.shape[0]
+        if rows is None:
+            rows = np.arange(T, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+        out = np.zeros((rows.shape[0], N), np.float64)
+        rc = self._lib.moda_oracle_kv_proj(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
+                                           T, Dm, N, _ptr(rows, ctypes.c_int64), rows.shape[0],
+                                           _ptr(out, ctypes.c_double))
+        if rc != 0:
+            raise ValueError(f"moda_oracle_kv_proj failed with {rc}")
+        return out
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -222,3 +250,7 @@ def forward(*args, **kw):
 
 def backward(*args, **kw):
     return default().backward(*args, **kw)
+
+
+def kv_proj(*args, **kw):
+    return default().kv_proj(*args, **kw)

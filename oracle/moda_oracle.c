@@ -456,3 +456,37 @@ int moda_oracle_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v
   free(jobs); free(priv);
   return status;
 }
+
+/*
+ * Depth key or value of an FFN layer.
+ *
+ * Where the depth KV comes from (reading notes, Sec. 二.3; summary, Sec. 2.2,
+ * the MoDA "write" step): attention layers append the K, V they already
+ * computed, while an FFN layer obtains its pair through a light KV projection
+ * of the FFN's INPUT X. MoDA keeps only the grouped depth key/value
+ * projections (no depth query). Plain reading: a linear map without bias,
+ *   out[r, n] = sum_{c < Dm} x[t_r, c] * w[n, c]     for n < N,
+ * with x [T, Dm], the weight one row per output feature, w [N, Dm], N = Hk*d
+ * (feature n = hk*d + j is element j of KV head hk), and t_r = rows[r].
+ * The sum is taken in double precision in the order of c and returned
+ * unrounded in out [n_rows, N]. The caller calls it once with W_K and once
+ * with W_V.
+ *
+ * Returns 0, or -1 on a bad argument.
+ */
+int moda_oracle_kv_proj(const uint16_t* x, const uint16_t* w, int T, int Dm, int N,
+                        const int64_t* rows, int64_t n_rows, double* out) {
+  if (!x || !w || !out || T < 1 || Dm < 1 || N < 1 || n_rows < 0) return -1;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int64_t t = rows ? rows[r] : r;
+    if (t < 0 || t >= T) return -1;
+    const uint16_t* xrow = x + t * (int64_t)Dm;
+    for (int n = 0; n < N; ++n) {
+      const uint16_t* wrow = w + (int64_t)n * Dm;
+      double s = 0.0;
+      for (int c = 0; c < Dm; ++c) s += bf16_to_double(xrow[c]) * bf16_to_double(wrow[c]);
+      out[r * (int64_t)N + n] = s;
+    }
+  }
+  return 0;
+}
