@@ -255,6 +255,8 @@ def main(argv=None):
                     help="timed moda_decode calls reported in the 'decode' object (0 = skip)")
     ap.add_argument("--bwd-steps", type=int, default=3,
                     help="timed moda_bwd calls reported in the 'bwd' object (0 = skip)")
+    ap.add_argument("--proj-steps", type=int, default=5,
+                    help="timed moda_kv_proj_write calls reported in the 'kv_proj' object (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=None,
                     help="seconds of oracle work for cpu_baseline (default 10) or per "
@@ -474,6 +476,47 @@ def main(argv=None):
                        "flops_counted": Fb, "fwd_plus_bwd_ms": fwd_ms + bwd_ms,
                        "kernels": "delta + depth (CUDA cores) + dq + dk/dv (tcgen05)"}
         del grads, delta, dO
+
+    # ---- an FFN layer's depth K/V: projection GEMM writing its slot (separate) ----
+    if args.proj_steps > 0 and w.L:
+        pw = wl.ProjWorkload(f"kv-proj-{w.name}", T=w.T, Dm=w.Hq * w.d, Hk=w.Hk, d=w.d, L=w.L,
+                             slot=w.L - 1)
+        g = torch.Generator(device=dev)
+        g.manual_seed(2)
+        xp = torch.randn((pw.T, pw.Dm), generator=g, device=dev).to(torch.bfloat16)
+        wk = (torch.randn((pw.Hk * pw.d, pw.Dm), generator=g, device=dev) / pw.Dm ** 0.5).to(torch.bfloat16)
+        wv = (torch.randn((pw.Hk * pw.d, pw.Dm), generator=g, device=dev) / pw.Dm ** 0.5).to(torch.bfloat16)
+        for _ in range(2):
+            moda.moda_kv_proj_write(xp, wk, wv, kd, vd, pw.slot, stream=stream)
+        ep = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.proj_steps)]
+        torch.cuda.synchronize(dev)
+        for a, b in ep:
+            a.record(stream)
+            moda.moda_kv_proj_write(xp, wk, wv, kd, vd, pw.slot, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        pms = statistics.median(a.elapsed_time(b) for a, b in ep)
+        # context: the same projection as two cuBLAS GEMMs plus two slot writes
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                moda.moda_depth_write((xp @ wk.t()).view(pw.T, pw.Hk, pw.d), kd, pw.slot, stream=stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.proj_steps):
+                moda.moda_depth_write((xp @ wk.t()).view(pw.T, pw.Hk, pw.d), kd, pw.slot, stream=stream)
+                moda.moda_depth_write((xp @ wv.t()).view(pw.T, pw.Hk, pw.d), vd, pw.slot, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ums = a.elapsed_time(b) / args.proj_steps
+        Fp = pw.flops()
+        line["kv_proj"] = {"ms": pms, "tflops": Fp / (pms * 1e-3) / 1e12,
+                           "pct_peak_burst": 100 * Fp / (pms * 1e-3) / 1e12 / peak,
+                           "shape": {"T": pw.T, "Dm": pw.Dm, "Hk": pw.Hk, "d": pw.d, "L": pw.L,
+                                     "slot": pw.slot},
+                           "flops_counted": Fp,
+                           "unfused_cublas_gemm_plus_slot_write_ms": ums}
+        del xp, wk, wv
 
     # ---- end to end: pinned host inputs in, o and lse out, every step ----
     if not args.no_e2e:

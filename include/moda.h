@@ -90,6 +90,32 @@ MODA_API moda_status moda_depth_write(const void* src, void* dst, int T, int Hk,
                                       int slot, moda_stream_t stream);
 
 /*
+ * moda_kv_proj_write -- an FFN layer's depth keys and values, projected from
+ * the FFN's input and written straight into slot `slot` of the packed depth
+ * streams (reading notes Sec. 二.3: the FFN branch adds a KV projection of its
+ * INPUT X; summary Sec. 2.2, "write" step: FFN layers get their pair from a
+ * light KV projection; MoDA keeps only the grouped depth K/V projections):
+ *
+ *   kd[hk][t][slot][j] = bf16( sum_c x[t][c] * wk[hk*d + j][c] )
+ *   vd[hk][t][slot][j] = bf16( sum_c x[t][c] * wv[hk*d + j][c] )
+ *
+ *   x       [T, Dm] bf16, the FFN's input rows
+ *   wk, wv  [Hk*d, Dm] bf16, one row per output feature (the layout of a
+ *           linear layer's weight); feature hk*d + j is element j of KV head hk
+ *   kd, vd  [Hk, T, L, d] bf16, the packed streams moda_fwd reads; only slot
+ *           `slot` (0 <= slot < L) is written, every other slot is left as is
+ * Arithmetic: bf16 products, fp32 accumulation over Dm, one rounding to bf16
+ * (nearest even). No bias: the pages name a projection and no more.
+ * Outputs must not overlap the inputs or each other. Supported: d in {64, 128},
+ * Dm a multiple of 64, 1 <= T <= 2^24, 1 <= L <= 1024.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA (synchronous); TIMEOUT
+ * via moda_get_device_error.
+ */
+MODA_API moda_status moda_kv_proj_write(const void* x, const void* wk, const void* wv, int T,
+                                        int Dm, int Hk, int d, int L, int slot, void* kd,
+                                        void* vd, moda_stream_t stream);
+
+/*
  * moda_fwd -- the MoDA forward (Sec. 2.2 joint softmax; Sec. 3.3 fused
  * kernel: group-aware query tiles, grouped causal mask, block-diagonal depth
  * mask, one online-softmax state).

@@ -24,7 +24,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_fwd", "moda_decode",
+EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_kv_proj_write", "moda_fwd", "moda_decode",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
@@ -57,6 +57,8 @@ def load():
         lib.moda_pack_depth.argtypes = [vp, vp, i, i, i, i, vp]
         lib.moda_pack_depth.restype = i
         lib.moda_depth_write.argtypes = [vp, vp, i, i, i, i, i, vp]
+        lib.moda_kv_proj_write.restype = i
+        lib.moda_kv_proj_write.argtypes = [vp, vp, vp] + [i] * 6 + [vp, vp, vp]
         lib.moda_depth_write.restype = i
         lib.moda_decode_workspace_bytes.argtypes = [i, i, i]
         lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -137,6 +139,25 @@ def moda_depth_write(src: torch.Tensor, dst: torch.Tensor, slot: int, stream=Non
     st = load().moda_depth_write(_ptr(src), _ptr(dst), T, Hk, d, L, int(slot), _stream(stream))
     _check(st, "moda_depth_write")
     return dst
+
+
+def moda_kv_proj_write(x: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor, kd: torch.Tensor,
+                       vd: torch.Tensor, slot: int, stream=None):
+    """An FFN layer's depth pair: K = x wk^T and V = x wv^T (bf16, fp32
+    accumulation) written into slot `slot` of the packed streams kd, vd
+    [Hk,T,L,d]. x is [T,Dm]; wk, wv are [Hk*d,Dm]. Returns (kd, vd)."""
+    for t, n in ((x, "x"), (wk, "wk"), (wv, "wv"), (kd, "kd"), (vd, "vd")):
+        _need(t, n)
+    T, Dm = x.shape
+    if kd.dim() != 4 or tuple(vd.shape) != tuple(kd.shape) or kd.shape[1] != T:
+        raise ValueError(f"kd and vd must both be [Hk,T,L,d] with T={T}")
+    Hk, _, L, d = kd.shape
+    if tuple(wk.shape) != (Hk * d, Dm) or tuple(wv.shape) != (Hk * d, Dm):
+        raise ValueError(f"wk and wv must be [{Hk * d},{Dm}]")
+    st = load().moda_kv_proj_write(_ptr(x), _ptr(wk), _ptr(wv), T, Dm, Hk, d, L, int(slot),
+                                   _ptr(kd), _ptr(vd), _stream(stream))
+    _check(st, "moda_kv_proj_write")
+    return kd, vd
 
 
 def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,

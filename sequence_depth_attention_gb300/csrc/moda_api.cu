@@ -146,6 +146,44 @@ moda_status moda_depth_write(const void* src, void* dst, int T, int Hk, int d, i
   return ok();
 }
 
+moda_status moda_kv_proj_write(const void* x, const void* wk, const void* wv, int T, int Dm,
+                               int Hk, int d, int L, int slot, void* kd, void* vd,
+                               moda_stream_t stream) {
+  if (!x || !wk || !wv || !kd || !vd) return fail(MODA_ERR_INVALID_ARG, "NULL input or output");
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (Hk < 1) return fail(MODA_ERR_INVALID_ARG, "Hk = %d < 1", Hk);
+  if (Dm < 1) return fail(MODA_ERR_INVALID_ARG, "Dm = %d < 1", Dm);
+  if (L < 1) return fail(MODA_ERR_INVALID_ARG, "L = %d < 1", L);
+  if (slot < 0 || slot >= L) return fail(MODA_ERR_INVALID_ARG, "slot = %d outside [0, %d)", slot, L);
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (Dm % 64 != 0) return fail(MODA_ERR_UNSUPPORTED, "Dm = %d is not a multiple of 64", Dm);
+  if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if ((int64_t)Hk * d > (1 << 24))
+    return fail(MODA_ERR_UNSUPPORTED, "Hk*d = %lld output features exceed 2^24", (long long)Hk * d);
+  const void* all[] = {x, wk, wv, kd, vd};
+  for (const void* p : all)
+    if (!aligned16(p)) return fail(MODA_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  const size_t xb = (size_t)T * Dm * 2, wb = (size_t)Hk * d * Dm * 2;
+  const size_t db = (size_t)Hk * T * L * d * 2;
+  const void* ins[] = {x, wk, wv};
+  const size_t insz[] = {xb, wb, wb};
+  for (int b = 0; b < 3; ++b)
+    if (overlaps(kd, db, ins[b], insz[b]) || overlaps(vd, db, ins[b], insz[b]))
+      return fail(MODA_ERR_INVALID_ARG, "an output overlaps an input");
+  if (overlaps(kd, db, vd, db)) return fail(MODA_ERR_INVALID_ARG, "kd and vd overlap");
+  moda::KvProjArgs a{};
+  a.x = x; a.wk = wk; a.wv = wv;
+  a.T = T; a.Dm = Dm; a.Hk = Hk; a.d = d; a.L = L; a.slot = slot;
+  a.kd = kd; a.vd = vd;
+  int dev;
+  moda_status st = device_state(&dev, &a.err, &a.num_sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_kv_proj(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "kv_proj launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, int T, int Hq, int Hk, int d, int L, float scale, void* o,
                      float* lse, moda_stream_t stream) {

@@ -51,6 +51,15 @@ struct DecodeArgs {
 };
 int decode_num_splits(int Tctx);
 
+// Arguments of one depth-KV projection after validation on the host.
+struct KvProjArgs {
+  const void *x, *wk, *wv;  // x [T, Dm]; wk, wv [Hk*d, Dm] (bf16)
+  int T, Dm, Hk, d, L, slot;
+  void *kd, *vd;            // packed [Hk, T, L, d] bf16; slot `slot` is written
+  unsigned int* err;
+  int num_sms;
+};
+
 // Kernel error codes latched into the device error word (first one wins).
 enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 
@@ -72,6 +81,7 @@ cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_tc(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_mma(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_kv_proj(const KvProjArgs& a, cudaStream_t stream);
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
                                int num_sms, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);

@@ -113,3 +113,49 @@ def sample_rows(T: int, Hq: int, G: int, n_random: int = 64, seed: int = 1):
     tt = np.repeat(np.array(ts, np.int64), Hq)
     hh = np.tile(np.arange(Hq, dtype=np.int64), len(ts))
     return tt, hh
+
+
+@dataclasses.dataclass(frozen=True)
+class ProjWorkload:
+    """Shape of one FFN layer's depth-KV projection: x [T, Dm] -> slot `slot`
+    of the packed [Hk, T, L, d] streams."""
+    name: str
+    T: int
+    Dm: int
+    Hk: int
+    d: int
+    L: int
+    slot: int
+    seed: int = 0
+
+    def flops(self) -> float:
+        """2 * T * Dm * (2 * Hk * d): the K and V products."""
+        return 2.0 * self.T * self.Dm * 2 * self.Hk * self.d
+
+
+# The long workload's layer: model width Dm = Hq * d = 16 * 128, Hk = 4, L = 48,
+# writing the last slot.
+PROJ_LONG = ProjWorkload("kv-proj-long-64k", T=65536, Dm=2048, Hk=4, d=128, L=48, slot=47)
+
+
+def make_proj_inputs(w: ProjWorkload, device="cpu", seed: int | None = None):
+    """x [T,Dm] ~ N(0,1); wk, wv [Hk*d,Dm] ~ N(0,1)/sqrt(Dm); kd, vd [Hk,T,L,d]
+    prefilled ~ N(0,1) (what earlier layers wrote). All bf16, drawn in the order
+    x, wk, wv, kd, vd from one generator seeded with ``seed`` (default w.seed)."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+
+    def draw(shape, mul=1.0):
+        x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+        if mul != 1.0:
+            x.mul_(mul)
+        return x.to(torch.bfloat16)
+
+    n = w.Hk * w.d
+    x = draw((w.T, w.Dm))
+    wk = draw((n, w.Dm), 1.0 / math.sqrt(w.Dm))
+    wv = draw((n, w.Dm), 1.0 / math.sqrt(w.Dm))
+    kd = draw((w.Hk, w.T, w.L, w.d))
+    vd = draw((w.Hk, w.T, w.L, w.d))
+    return {"x": x, "wk": wk, "wv": wv, "kd": kd, "vd": vd}

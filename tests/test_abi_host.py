@@ -146,6 +146,21 @@ def test_depth_write_rejects(lib, args, code):
     assert lib.moda_depth_write(*args, None) == code
 
 
+def _proj(lib, x=A, wk=B, wv=C, T=8, Dm=128, Hk=2, d=64, L=4, slot=1, kd=D, vd=E):
+    lib.moda_kv_proj_write.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 3
+    return lib.moda_kv_proj_write(x, wk, wv, T, Dm, Hk, d, L, slot, kd, vd, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), INVALID), (dict(vd=None), INVALID), (dict(T=0), INVALID), (dict(L=0), INVALID),
+    (dict(slot=4), INVALID), (dict(slot=-1), INVALID), (dict(Dm=96), UNSUPPORTED),
+    (dict(d=96), UNSUPPORTED), (dict(L=1025, slot=0), UNSUPPORTED), (dict(wk=B + 8), MISALIGNED),
+    (dict(kd=A), INVALID), (dict(vd=D + 64), INVALID),
+])
+def test_kv_proj_rejects(lib, kw, code):
+    assert _proj(lib, **kw) == code
+
+
 def test_decode_workspace_formula(lib):
     lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
     # (splits + 1) partials of (d + 2) floats per head; splits <= ceil(T/64), capped at 128
