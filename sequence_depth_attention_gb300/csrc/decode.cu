@@ -5,18 +5,21 @@
 // slots of the current token).
 //
 // HBM-bound: every cached K/V row is read once and used by the G query heads
-// of its KV head (about G flop per byte), so the work runs on CUDA cores.
+// of its KV head (about G flop per byte).
 //   pass 1  grid (nsplit + 1, Hk): CTA (s, hk) walks a contiguous chunk of the
 //           cache (the last CTA the depth slots) for the G heads of hk with
-//           an online softmax; TMA streams 64-key K and V boxes through a
-//           3-stage shared-memory ring while 8 warps (lanes split d) consume.
-//           Each writes a partial (m, l, unnormalised o) to the workspace.
+//           an online softmax; TMA streams 64-key K and V boxes (128-byte
+//           swizzle) through a shared-memory ring while 4 warps score 16 keys
+//           each on mma.sync tensor cores (the G heads are the rows of the A
+//           operand, so the dot products need no cross-lane reduction).
+//           Each CTA writes a partial (m, l, unnormalised o) to the workspace.
 //   pass 2  grid Hq: merge the nsplit + 1 partials of each head, o = O / l.
 #include <cuda_bf16.h>
 
 #include "moda_internal.h"
 #include "sm103.cuh"
 #include "tensor_map.h"
+#include "warp_mma.cuh"
 
 namespace moda {
 namespace {
@@ -24,48 +27,43 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// A lane's E = D/32 consecutive bf16 of a row, loaded in one access.
-template <int E> struct LaneRow;
-template <> struct LaneRow<4> {
-  using T = uint2;
-  __device__ static void unpack(const T& r, float* f) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  }
-};
-template <> struct LaneRow<2> {
-  using T = uint32_t;
-  __device__ static void unpack(const T& r, float* f) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r));
-    f[0] = a.x; f[1] = a.y;
-  }
-};
-
-// Keys of the CTA stream through a ring of kStages shared-memory stages of
-// kKB keys (K and V), filled by TMA (one elected thread) and tracked by
-// mbarriers, so kStages*kKB*d*4 bytes are in flight per CTA while its 8
-// warps work on the oldest stage: warp w takes keys w*kU .. w*kU+kU-1 of a
-// stage, lanes split d. A block-wide vote releases a stage, so a bounded
-// wait that gives up ends every thread of the CTA together.
-constexpr int kW = 8;       // warps
-constexpr int kKB = 64;     // keys per stage
-constexpr int kU = kKB / kW;
-constexpr int kStages = 3;
+// Keys of the CTA stream through a ring of NS shared-memory stages of kKB
+// keys (K and V), filled by TMA with the 128-byte swizzle (one elected thread)
+// and tracked by mbarriers. Warp w scores keys 16w .. 16w+15 of a stage on the
+// tensor cores (mma.sync m16n8k16): S = Q K^T with the G query heads of the
+// KV head as the rows of the A operand (rows >= G are zero) and K read by
+// ldmatrix, then an online softmax per row, then O += P V with P reused in
+// registers as the A operand and V read by ldmatrix.trans. A block-wide vote
+// releases a stage, so a bounded wait that gives up ends every thread of the
+// CTA together.
+constexpr int kW = 4;        // warps
+constexpr int kKB = 64;      // keys per stage
+constexpr int kKW = kKB / kW;  // keys per warp and stage (one k16 step of P V)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-template <int D, int G>
+template <int D>
 struct DecodeSmem {
+  static constexpr int kNS = D == 128 ? 3 : 4;    // stages
+  static constexpr int kBox = kKB * 128;          // one 64-column swizzled box of kKB rows
+  static constexpr int kTile = (D / 64) * kBox;   // K or V of one stage
   union {
-    __nv_bfloat16 kv[kStages][2][kKB][D];  // [stage][K or V][key][d] while streaming
-    struct {                                // the warps' states for the final merge
-      float o[kW][G][D];
-      float ml[kW][G][2];
+    uint8_t ring[kNS][2][kTile];  // [stage][K or V]
+    struct {                      // the warps' states for the final merge
+      float o[kW][16][D];
+      float ml[kW][16][2];
     } merge;
   } u;
-  uint64_t full[kStages];
+  uint64_t full[kNS];
   int abort;
 };
+
+// Byte offset of element (row, col) in a stage tile: 64-column boxes, 16-byte
+// chunks XOR-swizzled by (row & 7) inside each 1024-byte atom, the layout TMA
+// writes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz128(int row, int col) {
+  return (uint32_t)((col >> 6) * (kKB * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                    ((col & 7) << 1));
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kW * 32)
@@ -74,116 +72,132 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const __nv_bfloat16* __restrict__ q, int Tctx, int Hq, int L,
                     int keys_per_split, int nsplit, float scale_log2, float* __restrict__ part,
                     unsigned int* __restrict__ err) {
-  constexpr int E = D / 32;  // columns per lane
-  using Row = LaneRow<E>;
-  using RowT = typename Row::T;
+  using S = DecodeSmem<D>;
+  constexpr int NS = S::kNS;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  // TMA destinations need 128-byte alignment: align the base explicitly
-  DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  // 128-byte swizzled TMA destinations need 1024-byte alignment
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                ~static_cast<uintptr_t>(1023));
   const int split = blockIdx.x, hk = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool depth = split == nsplit;
   const int j0 = depth ? 0 : split * keys_per_split;
   const int j1 = depth ? L : min(Tctx, j0 + keys_per_split);
   const int nblk = (j1 - j0 + kKB - 1) / kKB;
-  constexpr uint32_t kStageBytes = 2u * kKB * D * 2u;
+  constexpr uint32_t kStageBytes = 2u * S::kTile;
 
   if (tid == 0) {
     sm.abort = 0;
-    for (int s = 0; s < kStages; ++s) sm103::mbar_init(sm103::smem_u32(&sm.full[s]), 1);
+    for (int s = 0; s < NS; ++s) sm103::mbar_init(sm103::smem_u32(&sm.full[s]), 1);
     sm103::fence_barrier_init();
   }
   __syncthreads();
-  auto issue = [&](int b) {  // block b -> stage b % kStages
-    const int s = b % kStages;
+  auto issue = [&](int b) {  // block b -> stage b % NS
+    const int s = b % NS;
     const uint32_t bar = sm103::smem_u32(&sm.full[s]);
     sm103::mbar_arrive_expect_tx(bar, kStageBytes);
-    const uint32_t dk = sm103::smem_u32(&sm.u.kv[s][0][0][0]);
-    const uint32_t dv = sm103::smem_u32(&sm.u.kv[s][1][0][0]);
     const int jb = j0 + b * kKB;
-    if (depth) {
-      sm103::tma_load_3d(dk, &tmKd, bar, 0, jb, hk);
-      sm103::tma_load_3d(dv, &tmVd, bar, 0, jb, hk);
-    } else {
-      sm103::tma_load_3d(dk, &tmK, bar, 0, hk, jb);
-      sm103::tma_load_3d(dv, &tmV, bar, 0, hk, jb);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      const uint32_t dk = sm103::smem_u32(&sm.u.ring[s][0][c * S::kBox]);
+      const uint32_t dv = sm103::smem_u32(&sm.u.ring[s][1][c * S::kBox]);
+      if (depth) {
+        sm103::tma_load_3d(dk, &tmKd, bar, c * 64, jb, hk);
+        sm103::tma_load_3d(dv, &tmVd, bar, c * 64, jb, hk);
+      } else {
+        sm103::tma_load_3d(dk, &tmK, bar, c * 64, hk, jb);
+        sm103::tma_load_3d(dv, &tmV, bar, c * 64, hk, jb);
+      }
     }
   };
   if (tid == 0)
-    for (int b = 0; b < min(kStages, nblk); ++b) issue(b);
+    for (int b = 0; b < min(NS, nblk); ++b) issue(b);
 
-  float qv[G][E];
+  // Q as the A operand (row r = query head hk*G + r, k = the head dimension)
+  const int r0 = lane >> 2, cq = (lane & 3) * 2;
+  uint32_t qa[D / 16][4];
+  {
+    auto ld = [&](int r, int c) -> uint32_t {
+      return r < G ? *reinterpret_cast<const uint32_t*>(q + (int64_t)(hk * G + r) * D + c) : 0u;
+    };
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float f[E];
-    Row::unpack(*reinterpret_cast<const RowT*>(q + (int64_t)(hk * G + g) * D + lane * E), f);
-#pragma unroll
-    for (int e = 0; e < E; ++e) qv[g][e] = f[e] * scale_log2;  // fold the scale into q
-  }
-  float m[G], l[G], o[G][E];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[g][e] = 0.f;
-  }
-  int issued = min(kStages, nblk);
-  for (int b = 0; b < nblk; ++b) {
-    const int s = b % kStages;
-    bool ok = sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[s]), (b / kStages) & 1,
-                                       &sm.abort, kTimeoutNs);
-    if (!__syncthreads_and(ok)) break;
-    const int jb = j0 + b * kKB + warp * kU;  // this warp's first key
-    float s_[G][kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      float kf[E];
-      Row::unpack(*reinterpret_cast<const RowT*>(&sm.u.kv[s][0][warp * kU + u][lane * E]), kf);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(qv[g][e], kf[e], acc);
-        s_[g][u] = acc;
-      }
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qa[ks][0] = ld(r0, ks * 16 + cq);
+      qa[ks][1] = ld(r0 + 8, ks * 16 + cq);
+      qa[ks][2] = ld(r0, ks * 16 + 8 + cq);
+      qa[ks][3] = ld(r0 + 8, ks * 16 + 8 + cq);
     }
+  }
+  float o[D / 8][4];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
+  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // rows r0 and r0 + 8, log2 units
+  float l0 = 0.f, l1 = 0.f;              // this lane's share of the row sums
+
+  // ldmatrix source rows of this lane: K (x4 = key halves x dimension halves
+  // of one k16 step), V (x4.trans = key halves x two 8-column groups)
+  const int kkey = warp * kKW + ((lane >> 4) << 3) + (lane & 7), kcol = ((lane >> 3) & 1) * 8;
+  const int vkey = warp * kKW + (((lane >> 3) & 1) << 3) + (lane & 7), vcol = (lane >> 4) * 8;
+
+  int issued = min(NS, nblk);
+  for (int b = 0; b < nblk; ++b) {
+    const int s = b % NS;
+    bool ok = sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[s]), (b / NS) & 1, &sm.abort,
+                                       kTimeoutNs);
+    if (!__syncthreads_and(ok)) break;
+    const int jw = j0 + b * kKB + warp * kKW;  // this warp's first key
+    if (jw < j1) {
+      const uint32_t kb = sm103::smem_u32(&sm.u.ring[s][0][0]);
+      const uint32_t vb = sm103::smem_u32(&sm.u.ring[s][1][0]);
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int u = 0; u < kU; ++u) s_[g][u] += __shfl_xor_sync(0xffffffffu, s_[g][u], off);
-    if (jb < j1) {  // the warp holds at least one valid key
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-        if (jb + u >= j1)
-#pragma unroll
-          for (int g = 0; g < G; ++g) s_[g][u] = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float mx = s_[g][0];
-#pragma unroll
-        for (int u = 1; u < kU; ++u) mx = fmaxf(mx, s_[g][u]);
-        const float mn = fmaxf(m[g], mx);
-        const float alpha = exp2f(m[g] - mn);
-        l[g] *= alpha;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[g][e] *= alpha;
-        m[g] = mn;
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t b00, b01, b10, b11;
+        wmma16::ldsm_x4(kb + swz128(kkey, ks * 16 + kcol), b00, b01, b10, b11);
+        wmma16::mma_bf16(c[0], qa[ks], b00, b01);
+        wmma16::mma_bf16(c[1], qa[ks], b10, b11);
       }
+      // scores in log2 units; keys at or past j1 do not exist
+      float sv[2][4];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        float vf[E];
-        Row::unpack(*reinterpret_cast<const RowT*>(&sm.u.kv[s][1][warp * kU + u][lane * E]), vf);
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float p = exp2f(s_[g][u] - m[g]);
-          l[g] += p;
+        for (int e = 0; e < 4; ++e)
+          sv[nt][e] = jw + nt * 8 + cq + (e & 1) < j1 ? c[nt][e] * scale_log2 : -INFINITY;
+      float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+      float mx1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+      const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+      m0 = n0;
+      m1 = n1;
+      float p[2][4];
 #pragma unroll
-          for (int e = 0; e < E; ++e) o[g][e] = fmaf(p, vf[e], o[g][e]);
-        }
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = exp2f(sv[nt][0] - ref0);
+        p[nt][1] = exp2f(sv[nt][1] - ref0);
+        p[nt][2] = exp2f(sv[nt][2] - ref1);
+        p[nt][3] = exp2f(sv[nt][3] - ref1);
+      }
+      l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+      l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+      uint32_t pa[4];
+      pa[0] = wmma16::pack_bf16(p[0][0], p[0][1]);
+      pa[1] = wmma16::pack_bf16(p[0][2], p[0][3]);
+      pa[2] = wmma16::pack_bf16(p[1][0], p[1][1]);
+      pa[3] = wmma16::pack_bf16(p[1][2], p[1][3]);
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        uint32_t v0, v1, v2, v3;
+        wmma16::ldsm_x4_t(vb + swz128(vkey, nd * 8 + vcol), v0, v1, v2, v3);
+        o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
+        o[nd + 1][0] *= a0; o[nd + 1][1] *= a0; o[nd + 1][2] *= a1; o[nd + 1][3] *= a1;
+        wmma16::mma_bf16(o[nd], pa, v0, v1);
+        wmma16::mma_bf16(o[nd + 1], pa, v2, v3);
       }
     }
     __syncthreads();  // stage s is free
@@ -192,24 +206,31 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       ++issued;
     }
   }
-  // in-flight copies land before the CTA exits (only after an abort)
+  // in-flight copies land before the ring is reused or the CTA exits
   if (tid == 0) {
     int never = 0;
-    for (int b = max(0, issued - kStages); b < issued; ++b)
-      sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[b % kStages]), (b / kStages) & 1, &never,
-                               kTimeoutNs);
+    for (int b = max(0, issued - NS); b < issued; ++b)
+      sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[b % NS]), (b / NS) & 1, &never, kTimeoutNs);
     if (sm.abort) atomicCAS(err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
   }
-  // merge the warps of the CTA (the ring is idle now: every copy has landed)
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   __syncthreads();
+  // merge the warps of the CTA through shared memory (the ring is idle now)
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) sm.u.merge.o[warp][g][lane * E + e] = o[g][e];
-    if (lane == 0) {
-      sm.u.merge.ml[warp][g][0] = m[g];
-      sm.u.merge.ml[warp][g][1] = l[g];
-    }
+  for (int nd = 0; nd < D / 8; ++nd) {
+    sm.u.merge.o[warp][r0][nd * 8 + cq] = o[nd][0];
+    sm.u.merge.o[warp][r0][nd * 8 + cq + 1] = o[nd][1];
+    sm.u.merge.o[warp][r0 + 8][nd * 8 + cq] = o[nd][2];
+    sm.u.merge.o[warp][r0 + 8][nd * 8 + cq + 1] = o[nd][3];
+  }
+  if ((lane & 3) == 0) {
+    sm.u.merge.ml[warp][r0][0] = m0;
+    sm.u.merge.ml[warp][r0][1] = l0;
+    sm.u.merge.ml[warp][r0 + 8][0] = m1;
+    sm.u.merge.ml[warp][r0 + 8][1] = l1;
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += kW * 32) {
@@ -314,21 +335,21 @@ cudaError_t launch_split(const DecodeArgs& a, int nsplit, int kps, cudaStream_t 
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.Tctx};
     const uint64_t str[2] = {row, row * a.Hk};
-    const uint32_t box[3] = {D, 1, kKB};
-    if (encode_bf16_plain(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (encode_bf16_plain(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const uint32_t box[3] = {64, 1, kKB};
+    if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   if (a.L > 0) {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.L, (uint64_t)a.Hk};
     const uint64_t str[2] = {row, (uint64_t)a.depth_hk_stride * 2};
-    const uint32_t box[3] = {D, kKB, 1};
-    if (encode_bf16_plain(&tkd, a.kd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (encode_bf16_plain(&tvd, a.vd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const uint32_t box[3] = {64, kKB, 1};
+    if (encode_bf16_sw128(&tkd, a.kd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   } else {
     tkd = tk;  // never read when L == 0
     tvd = tv;
   }
-  const size_t smem = sizeof(DecodeSmem<D, G>) + 128;
+  const size_t smem = sizeof(DecodeSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

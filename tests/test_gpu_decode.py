@@ -53,6 +53,8 @@ CASES = [
     Workload("dec-T257-G1", T=257, Hq=3, Hk=3, d=64, L=1),
     Workload("dec-T5000-G8", T=5000, Hq=16, Hk=2, d=128, L=24, seed=3),
     Workload("dec-T4096-G16", T=4096, Hq=16, Hk=1, d=128, L=96, seed=4),
+    Workload("dec-T65-G2", T=65, Hq=4, Hk=2, d=64, L=130, seed=9),
+    Workload("dec-T64-G2", T=64, Hq=6, Hk=3, d=128, L=64, seed=10),
 ]
 
 
