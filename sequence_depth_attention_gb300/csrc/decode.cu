@@ -112,6 +112,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   };
   if (tid == 0)
     for (int b = 0; b < min(NS, nblk); ++b) issue(b);
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Q as the A operand (row r = query head hk*G + r, k = the head dimension)
   const int r0 = lane >> 2, cq = (lane & 3) * 2;
@@ -269,6 +271,9 @@ decode_combine_kernel(const float* __restrict__ part, int nparts, int Hq,
   __shared__ float sm_o[kCombineWarps][D];
   __shared__ float sm_ml[kCombineWarps][2];
   const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float pm[kPartsPerWarp], pl[kPartsPerWarp], po[kPartsPerWarp][E];
 #pragma unroll
   for (int i = 0; i < kPartsPerWarp; ++i) {
@@ -376,8 +381,21 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
     default: e = launch_split<D, 16>(a, nsplit, kps, st); break;
   }
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<a.Hq, kCombineWarps * 32, 0, st>>>(a.work, nsplit + 1, a.Hq,
-                                                                (__nv_bfloat16*)a.o, a.lse);
+  // programmatic dependent launch: the combine CTAs become resident while the
+  // split kernel runs and start as soon as it completes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hq);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, (const float*)a.work, nsplit + 1, a.Hq,
+                         (__nv_bfloat16*)a.o, a.lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
