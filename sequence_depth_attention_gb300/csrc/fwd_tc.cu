@@ -25,14 +25,18 @@
 //
 // Roles (8 warps, one CTA per tile, longest tiles first):
 //   warp 0  lane 0: TMA producer for Q and the K blocks
-//   warp 1  lane 0: tcgen05.mma issuer; the whole warp allocates TMEM
+//   warp 1  lane 0: tcgen05.mma issuer of S = Q K^T; the whole warp allocates TMEM
 //   warp 2  lane 0: TMA producer for the V blocks
+//   warp 3  lane 0: tcgen05.mma issuer of O += P V
 //   warps 4-7     : softmax, one thread per tile row (= TMEM lane), and the
 //                   epilogue
 // TMEM (512 columns): S double buffer [0,128) [128,256), O [256, 256+d),
-// P (bf16 pairs) double buffer [384,448) [448,512). The MMA computes
-// S_{j+1} = Q K_{j+1}^T while the softmax turns S_j into P_j, then
-// O += P_j V_j with P read straight from TMEM.
+// P (bf16 pairs) [384,448), Q (bf16 pairs) [448, 448+d/2). The softmax warps
+// copy the tile's Q rows from shared memory into TMEM once, so S = Q K^T
+// reads only K from shared memory (an MMA with both operands in shared memory
+// would use the whole shared-memory read bandwidth and starve the TMA writes
+// of the next K/V blocks). The MMA computes S_{j+1} = Q K_{j+1}^T while the
+// softmax turns S_j into P_j, then O += P_j V_j with P read straight from TMEM.
 // The running max is rescaled lazily: O and l are rescaled only when a new
 // block raises the row max by more than 8 (a factor 256), which stays exact
 // because o = O / l uses the same reference for both.
@@ -63,29 +67,32 @@ template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;     // 64-column (128-byte) swizzle boxes per row
   static constexpr int kBoxBytes = 128 * 64 * 2;
-  static constexpr int kNSK = D == 128 ? 3 : 4;  // K stages
-  static constexpr int kNSV = D == 128 ? 3 : 4;  // V stages
+  static constexpr int kNSK = D == 128 ? 3 : 5;  // K stages in the K region
+  static constexpr int kNSV = D == 128 ? 3 : 6;  // V stages
+  // one more K stage lives in the Q region once Q has been copied to TMEM
+  static constexpr int kNSKT = kNSK + 1;
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kNSK * kKVBytes;
   static constexpr int kOffBar = kOffV + kNSV * kKVBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kColQ = 448;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct alignas(8) Barriers {
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4];
-  uint64_t v_full[4], v_empty[4];
+  uint64_t k_full[8], k_empty[8];
+  uint64_t v_full[8], v_empty[8];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t mma_done;
+  uint64_t q_tmem;
+  uint64_t mma_done, mma_done_pv;
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Barriers) <= 256, "barrier block");
+static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Params {
   int T, Hq, Hk, L, lgG, ntiles;
@@ -152,7 +159,7 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   if (tid == 0) {
     bars->abort = 0;
     mbar_init(smem_u32(&bars->q_full), 1);
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 8; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
       mbar_init(smem_u32(&bars->k_empty[s]), 1);
       mbar_init(smem_u32(&bars->v_full[s]), 1);
@@ -165,6 +172,8 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(smem_u32(&bars->pv_done[b]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
+    mbar_init(smem_u32(&bars->mma_done_pv), 1);
+    mbar_init(smem_u32(&bars->q_tmem), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -191,7 +200,7 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // issues the copies.
     const bool leader = elect_one();
     const bool is_k = warp == 0;
-    const int NS = is_k ? C::kNSK : C::kNSV;
+    const int NS = is_k ? C::kNSKT : C::kNSV;
     const uint32_t sbase = is_k ? sK : sV;
     const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
     const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
@@ -214,10 +223,12 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const int s = j % NS;
       const bool ok = mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs);
       if (!__all_sync(0xffffffffu, ok)) break;
+      // the K stage in the Q region is first written once Q sits in TMEM
+      if (is_k && j == C::kNSK && !warp_wait(smem_u32(&bars->q_tmem), 0, abort)) break;
       if (leader) {
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::kKVBytes);
-        const uint32_t dst = sbase + s * C::kKVBytes;
+        const uint32_t dst = (is_k && s == C::kNSK) ? sQ : sbase + s * C::kKVBytes;
         if (sch.depth) {
           for (int c = 0; c < C::kBoxes; ++c)
             tma_load_2d_hint(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + sch.index * BN,
@@ -238,88 +249,85 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (is_k) mbar_wait_bounded(smem_u32(&bars->q_full), 0, &never, kTimeoutNs);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------ MMA issuers
+    // Warp 1 issues the S = Q K^T products, warp 3 the O += P V products.
+    // Each waits for its own operands and commits its own MMAs, so the
+    // waits and fences of one overlap the other's MMAs on the tensor core.
     // The whole warp follows the pipeline so descriptors stay warp-uniform;
     // one elected lane issues tcgen05.mma / tcgen05.commit.
     const bool leader = elect_one();
-    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
-    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
-    // base descriptors; the start-address field (bits 0-13, 16-byte units)
-    // is advanced by adding byte offsets >> 4
-    const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t dk = sdesc_sw128(sK, 16, 1024);
-    const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);
-    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
-      return __all_sync(0xffffffffu, ok);
-    };
     // Two barriers checked in one round trip: lanes 0-15 poll a, 16-31 poll b.
     auto wait2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) -> bool {
       const bool lo = lane < 16;
       const bool ok = mbar_wait_bounded(smem_u32(lo ? a : b), lo ? pa : pb, abort, kTimeoutNs);
       return __all_sync(0xffffffffu, ok);
     };
-    // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
-    auto issue_s = [&](int j) {
-      const int s = j % C::kNSK;
-      if (leader) {
-        const uint64_t dks = dk + (uint64_t)((s * C::kKVBytes) >> 4);
-        const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
+    uint64_t* done = warp == 1 ? &bars->mma_done : &bars->mma_done_pv;
+    if (warp == 1) {
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+      // base descriptor; the start-address field (bits 0-13, 16-byte units)
+      // is advanced by adding byte offsets >> 4
+      const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+      // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
+      auto issue_s = [&](int j) {
+        const int s = j % C::kNSKT;
+        if (leader) {
+          const uint64_t dks = s == C::kNSK ? sdesc_sw128(sQ, 16, 1024)
+                                            : dk + (uint64_t)((s * C::kKVBytes) >> 4);
+          const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(dcol, dq + off, dks + off, idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ts(dcol, tbase + C::kColQ + kk * 8, dks + off, idS, kk > 0);
+          }
+          tc_commit(smem_u32(&bars->k_empty[s]));
+          tc_commit(smem_u32(&bars->s_full[j & 1]));
         }
-        tc_commit(smem_u32(&bars->k_empty[s]));
-        tc_commit(smem_u32(&bars->s_full[j & 1]));
-      }
-      __syncwarp();
-    };
-    // Issue order: S_0, S_1, then per block j: S_{j+2} as soon as the
-    // softmax has read S_j out of its buffer, and PV_j once P_j is ready.
-    // S_{j+2} thus runs on the tensor core while the softmax works on j.
-    bool ok = wait2(&bars->q_full, 0, &bars->k_full[0], 0);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-    }
-    if (ok && nb > 1) {
-      ok = wait(&bars->k_full[1 % C::kNSK], (1 / C::kNSK) & 1);
+        __syncwarp();
+      };
+      // S_0, S_1, then S_{j+2} as soon as the softmax has read S_j out of
+      // its buffer: S_{j+2} runs on the tensor core while the softmax works on j
+      bool ok = wait2(&bars->q_tmem, 0, &bars->k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(1);
+        issue_s(0);
       }
-    }
-    for (int j = 0; ok && j < nb; ++j) {
-      const int sb = j & 1;
-      if (j + 2 < nb) {
-        const int ks = (j + 2) % C::kNSK;
-        if (!wait2(&bars->s_free[sb], (j >> 1) & 1, &bars->k_full[ks], ((j + 2) / C::kNSK) & 1))
+      for (int j = 1; ok && j < nb; ++j) {
+        const int ks = j % C::kNSKT;
+        if (j >= 2) {
+          if (!wait2(&bars->s_free[j & 1], ((j - 2) >> 1) & 1, &bars->k_full[ks], (j / C::kNSKT) & 1)) break;
+        } else if (!wait2(&bars->k_full[ks], (j / C::kNSKT) & 1, &bars->k_full[ks], (j / C::kNSKT) & 1)) {
           break;
+        }
         tc_fence_after();
-        issue_s(j + 2);
+        issue_s(j);
       }
-      const int vs = j % C::kNSV;
-      if (!wait2(&bars->p_full[sb], (j >> 1) & 1, &bars->v_full[vs], (j / C::kNSV) & 1)) break;
-      tc_fence_after();
-      if (leader) {
-        const uint64_t dvs = dv + (uint64_t)((vs * C::kKVBytes) >> 4);
-        const uint32_t pcol = tbase + C::kColP + sb * 64;
+    } else {
+      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
+      const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);
+      for (int j = 0; j < nb; ++j) {
+        const int sb = j & 1, vs = j % C::kNSV;
+        if (!wait2(&bars->p_full[sb], (j >> 1) & 1, &bars->v_full[vs], (j / C::kNSV) & 1)) break;
+        tc_fence_after();
+        if (leader) {
+          const uint64_t dvs = dv + (uint64_t)((vs * C::kKVBytes) >> 4);
+          const uint32_t pcol = tbase + C::kColP;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase + C::kColO, pcol + kk * 8, dvs + (uint64_t)((kk * 2048) >> 4), idPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&bars->v_empty[vs]));
-        tc_commit(smem_u32(&bars->pv_done[sb]));
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tbase + C::kColO, pcol + kk * 8, dvs + (uint64_t)((kk * 2048) >> 4), idPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&bars->v_empty[vs]));
+          tc_commit(smem_u32(&bars->pv_done[sb]));
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
     // every MMA issued by this warp has completed before TMEM is freed
     if (leader) {
       int never = 0;
-      tc_commit(smem_u32(&bars->mma_done));
-      mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);
+      tc_commit(smem_u32(done));
+      mbar_wait_bounded(smem_u32(done), 0, &never, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -336,8 +344,29 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const float sl = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // Q row -> TMEM columns [kColQ, kColQ + d/2) as bf16 pairs in row order, the
+    // A operand of S = Q K^T (so the MMA reads only K from shared memory)
+    if (!warp_wait(smem_u32(&bars->q_full), 0, abort)) ok = false;
+    if (ok) {
+      const uint8_t* qrow = smem + C::kOffQ + row * 128;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * C::kBoxBytes + ((k ^ (row & 7)) << 4));
+          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        }
+        tmem_st32(tmem_addr(tbase, lane_base, C::kColQ + c * 32), w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      // the Q region becomes a K stage (TMA writes): order these reads first
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&bars->q_tmem));
+    }
     Sched sch;
-    for (int j = 0; j < nb; ++j) {
+    for (int j = 0; ok && j < nb; ++j) {
       sch.next(n_depth, nb);
       const int sb = j & 1;
       if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort)) {
@@ -457,9 +486,11 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         sum = compute_p(m_ref);
       }
       l += sum;
-      // P_j reuses the buffer of P_{j-2}: the tensor core must have consumed it
-      if (j >= 2) {
-        if (!warp_wait(smem_u32(&bars->pv_done[sb]), ((j - 2) >> 1) & 1, abort)) {
+      // P_j overwrites P_{j-1}: the tensor core must have consumed it (the
+      // slow path above may have waited for it already; the phase test is
+      // idempotent)
+      if (j >= 1) {
+        if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
           ok = false;
           break;
         }
@@ -467,7 +498,7 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c)
-        tmem_st32(tmem_addr(tbase, lane_base, C::kColP + sb * 64 + c * 32), pk + c * 32);
+        tmem_st32(tmem_addr(tbase, lane_base, C::kColP + c * 32), pk + c * 32);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[sb]));
