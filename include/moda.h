@@ -58,13 +58,18 @@ typedef enum {
  *
  *   dst[hk][t][l][c] = src[l][t][hk][c]      (bit-exact copy)
  *
- *   src  [L, T, Hk, d] bf16 -- slot l is what the l-th earlier layer appended
- *   dst  [Hk, T, L, d] bf16 -- must not overlap src
+ *   src  [L, T, Hk, d] bf16 -- slot l is what the l-th earlier layer appended;
+ *        device memory, or page-locked host memory mapped into the device
+ *        address space (cudaHostAlloc / cudaHostRegister): the kernel then
+ *        reads it over the host link, so the host-to-device transfer and the
+ *        relayout are one pass
+ *   dst  [Hk, T, L, d] bf16 device memory -- must not overlap src
  *   d    64 or 128
  * Call once for the depth keys and once for the depth values. L == 0 is a
  * no-op (src and dst may then be NULL).
- * Errors: INVALID_ARG (NULL with L > 0, T < 1, Hk < 1, L < 0, src == dst),
- * UNSUPPORTED (d), MISALIGNED, CUDA.
+ * Errors: INVALID_ARG (NULL with L > 0, T < 1, Hk < 1, L < 0, src == dst,
+ * pageable host memory or an address the device cannot reach), UNSUPPORTED (d),
+ * MISALIGNED, CUDA.
  */
 MODA_API moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                             int d, moda_stream_t stream);

@@ -115,11 +115,22 @@ def _need(t, name, dtype=torch.bfloat16):
 
 
 def moda_pack_depth(src: torch.Tensor, dst: torch.Tensor | None = None, stream=None):
-    """[L,T,Hk,d] -> [Hk,T,L,d] (bit-exact). Returns dst."""
-    _need(src, "src")
+    """[L,T,Hk,d] -> [Hk,T,L,d] (bit-exact). Returns dst.
+
+    src may be a CUDA tensor or a pinned (page-locked) CPU tensor; the kernel
+    then reads it over the host link, so the transfer and the relayout are one
+    pass. dst is always a CUDA tensor."""
+    if src.is_cuda:
+        _need(src, "src")
+    else:
+        if not isinstance(src, torch.Tensor) or src.dtype != torch.bfloat16 or not src.is_contiguous():
+            raise TypeError("src: expected a contiguous bf16 tensor")
+        if not src.is_pinned():
+            raise ValueError("src: a CPU tensor must be pinned (page-locked)")
     L, T, Hk, d = src.shape
     if dst is None:
-        dst = torch.empty((Hk, T, L, d), dtype=src.dtype, device=src.device)
+        dev = src.device if src.is_cuda else torch.device("cuda", torch.cuda.current_device())
+        dst = torch.empty((Hk, T, L, d), dtype=src.dtype, device=dev)
     _need(dst, "dst")
     if tuple(dst.shape) != (Hk, T, L, d):
         raise ValueError(f"dst: expected shape {(Hk, T, L, d)}, got {tuple(dst.shape)}")

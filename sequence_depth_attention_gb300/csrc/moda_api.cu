@@ -103,6 +103,28 @@ const char* moda_status_string(moda_status s) {
 
 const char* moda_last_error_detail(void) { return g_detail; }
 
+// The address a kernel must use for p: p itself for device or managed memory,
+// the device mapping for page-locked host memory; nullptr (and the reason)
+// for memory the device cannot address, such as pageable host memory.
+static const void* device_view(const void* p, bool allow_host, const char** why) {
+  cudaPointerAttributes at;
+  const cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    *why = "the runtime does not know this address";
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeHost && allow_host) {
+    if (at.devicePointer) return at.devicePointer;
+    *why = "page-locked host memory without a device mapping";
+    return nullptr;
+  }
+  *why = at.type == cudaMemoryTypeHost ? "host memory where device memory is required"
+                                       : "pageable host memory (page-lock it, or copy it to the device)";
+  return nullptr;
+}
+
 moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk, int d,
                             moda_stream_t stream) {
   if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
@@ -119,7 +141,11 @@ moda_status moda_pack_depth(const void* src, void* dst, int L, int T, int Hk, in
   unsigned int* err;
   moda_status st = device_state(&dev, &err, &sms);
   if (st != MODA_OK) return st;
-  cudaError_t e = moda::launch_pack_depth(src, dst, L, T, Hk, d, (cudaStream_t)stream);
+  const char* why = "";
+  const void* ksrc = device_view(src, true, &why);
+  if (!ksrc) return fail(MODA_ERR_INVALID_ARG, "src: %s", why);
+  if (!device_view(dst, false, &why)) return fail(MODA_ERR_INVALID_ARG, "dst: %s", why);
+  cudaError_t e = moda::launch_pack_depth(ksrc, dst, L, T, Hk, d, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "pack_depth launch: %s", cudaGetErrorString(e));
   return ok();
 }
