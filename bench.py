@@ -257,6 +257,8 @@ def main(argv=None):
                     help="timed moda_bwd calls reported in the 'bwd' object (0 = skip)")
     ap.add_argument("--proj-steps", type=int, default=5,
                     help="timed moda_kv_proj_write calls reported in the 'kv_proj' object (0 = skip)")
+    ap.add_argument("--variant-steps", type=int, default=3,
+                    help="timed moda_fwd_depth_cc calls for the 'depth_variant' object (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=None,
                     help="seconds of oracle work for cpu_baseline (default 10) or per "
@@ -394,6 +396,28 @@ def main(argv=None):
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
+
+    # ---- the depth variant choice: CUDA-core depth in a second pass ----
+    if w.L and args.variant_steps > 0:
+        moda.moda_fwd(q, k, v, kd, vd, w.scale, o=o, lse=lse, stream=stream,
+                      depth_on_cuda_cores=True)
+        ec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.variant_steps)]
+        torch.cuda.synchronize(dev)
+        for a, b in ec:
+            a.record(stream)
+            moda.moda_fwd(q, k, v, kd, vd, w.scale, o=o, lse=lse, stream=stream,
+                          depth_on_cuda_cores=True)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        cc_ms = statistics.median(a.elapsed_time(b) for a, b in ec)
+        line["depth_variant"] = {
+            "tensor_core_depth_ms": fwd_ms, "cuda_core_depth_ms": cc_ms,
+            "L0_ms": fwd0_ms, "tensor_core_depth_cost_ms": fwd_ms - fwd0_ms,
+            "cuda_core_depth_cost_ms": cc_ms - fwd0_ms,
+            "chosen": "tensor cores (moda_fwd)" if fwd_ms <= cc_ms else "cuda cores",
+            "note": "cuda-core variant = moda_fwd_depth_cc: the L=0 forward, then one warp per "
+                    "(KV head, position) scoring its L slots and merging into o and lse"}
 
     # ---- layer-by-layer depth writes (the model path that replaces the pack) ----
     if w.L:

@@ -155,6 +155,25 @@ MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
                      moda_stream_t stream);
 
 /*
+ * moda_fwd_depth_cc -- the same result as moda_fwd, with the depth slots on
+ * CUDA cores instead of tensor cores: the sequence part runs as moda_fwd with
+ * L = 0, then one warp per (KV head, position) reads that position's L slots
+ * (16-byte loads of the packed rows), scores them for the G heads of the group
+ * and merges its softmax state exactly into o and lse (the joint softmax of
+ * Sec. 2.2 split into its sequence and depth halves, lse = log(e^lse_seq +
+ * e^lse_depth)). It is the measured alternative to moda_fwd's depth blocks
+ * under the block-diagonal mask of Sec. 3.3; moda_fwd is the faster of the two
+ * on the measured shapes.
+ * Arguments, layouts and errors as moda_fwd, except that lse is required
+ * (it carries the sequence part's state into the merge). Probabilities of
+ * depth slots stay fp32 here (moda_fwd rounds P to bf16 for the MMA).
+ */
+MODA_API moda_status moda_fwd_depth_cc(const void* q, const void* k, const void* v,
+                                       const void* kd, const void* vd, int T, int Hq, int Hk,
+                                       int d, int L, float scale, void* o, float* lse,
+                                       moda_stream_t stream);
+
+/*
  * moda_decode -- one decoding step: the new token at position t = Tctx - 1
  * attends, under one softmax, to the sequence KV cache (positions 0..t, its
  * own K/V included) and to the L depth slots of position t (Sec. 2.2; the

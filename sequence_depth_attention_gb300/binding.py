@@ -24,7 +24,8 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_kv_proj_write", "moda_fwd", "moda_decode",
+EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_kv_proj_write", "moda_fwd",
+           "moda_fwd_depth_cc", "moda_decode",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
@@ -66,6 +67,8 @@ def load():
                                                                            ctypes.c_size_t, vp]
         lib.moda_decode.restype = i
         lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
+        lib.moda_fwd_depth_cc.restype = i
+        lib.moda_fwd_depth_cc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
         lib.moda_bwd.restype = i
@@ -172,9 +175,13 @@ def moda_kv_proj_write(x: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor, kd: 
 
 
 def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
-             want_lse: bool = True):
+             want_lse: bool = True, depth_on_cuda_cores: bool = False):
     """MoDA forward. q[T,Hq,d], k/v[T,Hk,d], kd/vd packed [Hk,T,L,d] (or
-    None when L == 0). Returns (o[T,Hq,d] bf16, lse[T,Hq] fp32 or None)."""
+    None when L == 0). Returns (o[T,Hq,d] bf16, lse[T,Hq] fp32 or None).
+    depth_on_cuda_cores=True calls moda_fwd_depth_cc (same result, the depth
+    slots on CUDA cores in a second pass; lse is then always produced)."""
+    if depth_on_cuda_cores:
+        want_lse = True
     _need(q, "q"), _need(k, "k"), _need(v, "v")
     T, Hq, d = q.shape
     Hk = k.shape[1]
@@ -197,9 +204,11 @@ def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     if lse is not None:
         _need(lse, "lse", torch.float32)
-    st = load().moda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L,
-                         float(scale), _ptr(o), _ptr(lse), _stream(stream))
-    _check(st, "moda_fwd")
+    fn, name = (load().moda_fwd_depth_cc, "moda_fwd_depth_cc") if depth_on_cuda_cores else \
+        (load().moda_fwd, "moda_fwd")
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L, float(scale), _ptr(o),
+            _ptr(lse), _stream(stream))
+    _check(st, name)
     return o, lse
 
 

@@ -210,9 +210,10 @@ moda_status moda_kv_proj_write(const void* x, const void* wk, const void* wv, in
   return ok();
 }
 
-moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,
-                     const void* vd, int T, int Hq, int Hk, int d, int L, float scale, void* o,
-                     float* lse, moda_stream_t stream) {
+// Validation shared by the forward entry points; fills *out on success.
+static moda_status prepare_fwd(const void* q, const void* k, const void* v, const void* kd,
+                               const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
+                               void* o, float* lse, moda::FwdArgs* out) {
   if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL q, k, v or o");
   if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
   if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
@@ -243,15 +244,42 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   }
   if (overlaps(o, qb, lse, lb)) return fail(MODA_ERR_INVALID_ARG, "o and lse overlap");
 
-  moda::FwdArgs a{};
+  moda::FwdArgs& a = *out;
+  a = moda::FwdArgs{};
   a.q = q; a.k = k; a.v = v;
   a.kd = L ? kd : nullptr; a.vd = L ? vd : nullptr;
   a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G;
   a.scale = scale; a.o = o; a.lse = lse;
-  moda_status st = device_state(&a.device, &a.err, &a.num_sms);
+  return device_state(&a.device, &a.err, &a.num_sms);
+}
+
+moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, int T, int Hq, int Hk, int d, int L, float scale, void* o,
+                     float* lse, moda_stream_t stream) {
+  moda::FwdArgs a;
+  moda_status st = prepare_fwd(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, &a);
   if (st != MODA_OK) return st;
   cudaError_t e = moda::launch_fwd_tc(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_fwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_fwd_depth_cc(const void* q, const void* k, const void* v, const void* kd,
+                              const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
+                              void* o, float* lse, moda_stream_t stream) {
+  if (!lse) return fail(MODA_ERR_INVALID_ARG, "lse is required (it carries the merge state)");
+  moda::FwdArgs a;
+  moda_status st = prepare_fwd(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, &a);
+  if (st != MODA_OK) return st;
+  // pass 1: the sequence part alone (the forward with L = 0)
+  moda::FwdArgs seq = a;
+  seq.L = 0;
+  seq.kd = seq.vd = nullptr;
+  cudaError_t e = moda::launch_fwd_tc(seq, (cudaStream_t)stream);
+  // pass 2: the depth slots on CUDA cores, merged into o and lse
+  if (e == cudaSuccess && a.L > 0) e = moda::launch_fwd_depth_cc(a, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(MODA_ERR_CUDA, "moda_fwd_depth_cc launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -72,6 +72,8 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
+// Depth part on CUDA cores, merged into o and lse that hold the L = 0 result.
+cudaError_t launch_fwd_depth_cc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // The sequence share of dq, added to what the depth kernel wrote (L > 0) or
 // written (L == 0): tcgen05 version (dispatched) and mma.sync version.

@@ -25,7 +25,7 @@ def ensure_built():
     moda.load()
 
 
-def run_cuda(x, scale, device="cuda"):
+def run_cuda(x, scale, device="cuda", depth_on_cuda_cores=False):
     """x: dict of bf16 tensors (kd/vd in [L,T,Hk,d]). Returns o, lse on CPU."""
     q, k, v = (x[n].to(device) for n in ("q", "k", "v"))
     L = x["kd"].shape[0]
@@ -34,7 +34,7 @@ def run_cuda(x, scale, device="cuda"):
         vd = moda.moda_pack_depth(x["vd"].to(device))
     else:
         kd = vd = None
-    o, lse = moda.moda_fwd(q, k, v, kd, vd, scale)
+    o, lse = moda.moda_fwd(q, k, v, kd, vd, scale, depth_on_cuda_cores=depth_on_cuda_cores)
     torch.cuda.synchronize()
     assert moda.moda_get_device_error() == 0
     return o.float().cpu().numpy(), lse.cpu().numpy()
@@ -59,11 +59,12 @@ def compare(x, scale, o, lse, ts=None, hs=None):
     return eo, el
 
 
-def check_workload(w: Workload, sampled=False, device_inputs=False, q_mul=1.0):
+def check_workload(w: Workload, sampled=False, device_inputs=False, q_mul=1.0,
+                   depth_on_cuda_cores=False):
     x = make_inputs(w, device="cuda" if device_inputs else "cpu")
     if q_mul != 1.0:
         x["q"] = (x["q"].float() * q_mul).to(torch.bfloat16)
-    o, lse = run_cuda(x, w.scale)
+    o, lse = run_cuda(x, w.scale, depth_on_cuda_cores=depth_on_cuda_cores)
     if device_inputs:
         x = {n: t.cpu() for n, t in x.items()}
     assert np.isfinite(o).all() and np.isfinite(lse).all()

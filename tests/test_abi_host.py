@@ -85,6 +85,19 @@ def test_fwd_rejects(lib, kw, code):
     assert lib.moda_last_error_detail().decode() != ""
 
 
+def fwd_cc(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.125, o=O, lse=LSE):
+    return lib.moda_fwd_depth_cc(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lse=None), INVALID), (dict(q=None), INVALID), (dict(d=96), UNSUPPORTED),
+    (dict(Hq=6, Hk=2), UNSUPPORTED), (dict(kd=D + 2), MISALIGNED), (dict(o=A), INVALID),
+])
+def test_fwd_depth_cc_rejects(lib, kw, code):
+    # the CUDA-core depth variant validates exactly like moda_fwd, and needs lse
+    assert fwd_cc(lib, **kw) == code
+
+
 def test_fwd_l0_accepts_null_depth(lib):
     # L = 0 with NULL kd/vd passes validation; without a GPU it stops at the
     # device check, with one it would run (covered by the GPU tests).
