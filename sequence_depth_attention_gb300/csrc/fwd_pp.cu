@@ -1,0 +1,529 @@
+// MoDA forward for d = 64: two query tiles per CTA in ping-pong (sm_103a).
+//
+// Same method and tiling as the d = 128 kernel (fwd_tc.cu): G-stacked
+// 128-row query tiles, 128-key sequence blocks under the grouped causal mask,
+// depth blocks under the block-diagonal mask, one online softmax per row.
+// At d = 64 a block costs the tensor core half as much while its softmax costs
+// the same, so one tile per CTA leaves the tensor core idle most of the time.
+// Here a CTA owns two adjacent tiles A and B of one KV head (positions
+// [p0, p0+P) and [p0+P, p0+2P), P = 128/G): they read the same K/V blocks,
+// which are staged once, and each tile has its own softmax warpgroup and its
+// own MMA issuer, so one tile's softmax overlaps the other tile's MMAs.
+//
+// Roles (12 warps): warp 0 TMA for Q_A, Q_B and the K blocks; warp 2 TMA for
+// the V blocks; warp 1 issues tile A's MMAs, warp 3 tile B's; warps 4-7 are
+// tile A's softmax and epilogue, warps 8-11 tile B's (thread = row = TMEM
+// lane). TMEM: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384),
+// P_A [384,448), P_B [448,512). Each issuer runs its S stream one used block
+// ahead of its P.V stream: S_X(j+1) once the softmax holds S_X(j) in
+// registers, P_X(j).V(j) once P_X(j) is stored.
+// A block may be used by A, B or both (the last sequence block, and the
+// depth blocks, which hold one tile's positions or both). Every K/V stage is
+// released by two arrivals per block, one per tile: the MMA commit of a tile
+// that used the block, or a plain arrive of one that did not, made only
+// after the block's full barrier, so an early arrival never completes the
+// previous block's phase.
+// The softmax warpgroups get 216 registers each and the TMA/MMA warpgroup 64
+// (128 x 64 + 256 x 216 = 63488, within the launch allocation of 384 x 168).
+// Every wait is bounded (2 s); on expiry the CTA drains, frees TMEM and
+// latches MODA_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+
+#include "moda_internal.h"
+#include "sm103.cuh"
+#include "tensor_map.h"
+
+namespace moda {
+namespace {
+
+using namespace sm103;
+
+constexpr int D = 64;
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int kThreads = 384;
+constexpr int kNS = 6;  // K and V stages
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr int kTile = 128 * D * 2;  // one 128-row, 64-column box (16 KB)
+constexpr int kOffQ = 0;            // Q_A, Q_B
+constexpr int kOffK = 2 * kTile;
+constexpr int kOffV = kOffK + kNS * kTile;
+constexpr int kOffBar = kOffV + kNS * kTile;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+
+struct alignas(8) PpBars {
+  uint64_t q_full;
+  uint64_t k_full[kNS], k_empty[kNS];
+  uint64_t v_full[kNS], v_empty[kNS];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // per tile
+  uint64_t mma_done[2];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PpBars) <= 512, "barrier block");
+
+struct PpParams {
+  int T, Hq, Hk, L, lgG, npairs;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The pair's blocks in order: the n_depth depth blocks spread among the
+// sequence blocks (Bresenham), and which tiles use each.
+struct PairSched {
+  int acc = 0, db = 0, sbk = 0;
+  bool depth = false;
+  int index = 0;
+  __device__ void next(int n_depth, int nb) {
+    acc += n_depth;
+    depth = acc >= nb;
+    if (depth) {
+      acc -= nb;
+      index = db++;
+    } else {
+      index = sbk++;
+    }
+  }
+};
+
+struct PairGeom {
+  int P;        // positions per tile
+  int p0;       // first position of tile A (tile B starts at p0 + P)
+  int npos[2];  // positions of A and B (0: B absent)
+  int nb_seq[2];
+  int n_depth, nb;
+  __device__ bool uses(int x, const PairSched& s, int L) const {
+    if (npos[x] == 0) return false;
+    if (!s.depth) return s.index < nb_seq[x];
+    const int r0 = s.index * BN, r1 = r0 + BN;  // pair-relative depth rows of the block
+    const int lo = x * P * L, hi = lo + npos[x] * L;
+    return r0 < hi && r1 > lo;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKd,
+                   const __grid_constant__ CUtensorMap tmVd, const PpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  PpBars* bars = reinterpret_cast<PpBars*>(smem + kOffBar);
+  const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = 1 << p.lgG;
+  PairGeom g;
+  g.P = BM >> p.lgG;
+  const int pp = p.npairs - 1 - (int)(blockIdx.x / p.Hk);  // longest pair first
+  const int hk = (int)(blockIdx.x % p.Hk);
+  g.p0 = pp * 2 * g.P;
+  g.npos[0] = min(g.P, p.T - g.p0);
+  g.npos[1] = g.p0 + g.P < p.T ? min(g.P, p.T - g.p0 - g.P) : 0;
+  for (int x = 0; x < 2; ++x)
+    g.nb_seq[x] = g.npos[x] ? (g.p0 + x * g.P + g.npos[x] - 1) / BN + 1 : 0;
+  const int nd = (g.npos[0] + g.npos[1]) * p.L;  // the pair's packed depth rows
+  g.n_depth = (nd + BN - 1) / BN;
+  g.nb = g.n_depth + max(g.nb_seq[0], g.nb_seq[1]);
+  const int depth_row0 = (hk * p.T + g.p0) * p.L;
+
+  if (tid == 0) {
+    bars->abort = 0;
+    mbar_init(smem_u32(&bars->q_full), 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(smem_u32(&bars->k_full[s]), 1);
+      mbar_init(smem_u32(&bars->k_empty[s]), 2);  // one arrival per tile and block
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 2);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bars->s_full[x]), 1);
+      mbar_init(smem_u32(&bars->s_free[x]), 128);
+      mbar_init(smem_u32(&bars->p_full[x]), 128);
+      mbar_init(smem_u32(&bars->pv_done[x]), 1);
+      mbar_init(smem_u32(&bars->mma_done[x]), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    if (p.L) {
+      tma_prefetch_desc(&tmKd);
+      tma_prefetch_desc(&tmVd);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------- TMA producers
+      const bool leader = elect_one();
+      const bool is_k = warp == 0;
+      const uint32_t sbase = is_k ? sK : sV;
+      const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
+      const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      const uint64_t pol_once = l2_policy_evict_first();
+      if (is_k && leader) {
+        const uint32_t qb = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qb, (g.npos[1] ? 2 : 1) * kTile);
+        tma_load_3d_hint(sQ, &tmQ, qb, 0, hk * G, g.p0, pol_once);
+        if (g.npos[1]) tma_load_3d_hint(sQ + kTile, &tmQ, qb, 0, hk * G, g.p0 + g.P, pol_once);
+      }
+      int issued = 0;
+      PairSched sch;
+      for (int j = 0; j < g.nb; ++j) {
+        sch.next(g.n_depth, g.nb);
+        const int s = j % kNS;
+        if (!warp_wait(smem_u32(&empty[s]), ((j / kNS) & 1) ^ 1, abort)) break;
+        if (leader) {
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, kTile);
+          const uint32_t dst = sbase + s * kTile;
+          if (sch.depth)
+            tma_load_2d_hint(dst, dep_map, fb, 0, depth_row0 + sch.index * BN, pol_once);
+          else
+            tma_load_3d(dst, seq_map, fb, 0, hk, sch.index * BN);
+        }
+        __syncwarp();
+        issued = j + 1;
+      }
+      if (leader) {  // every copy this warp issued lands before shared memory is released
+        int never = 0;
+        for (int j = max(0, issued - kNS); j < issued; ++j)
+          mbar_wait_bounded(smem_u32(&full[j % kNS]), (j / kNS) & 1, &never, kTimeoutNs);
+        if (is_k) mbar_wait_bounded(smem_u32(&bars->q_full), 0, &never, kTimeoutNs);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------- MMA issuers
+      // warp 1 issues tile A's MMAs, warp 3 tile B's. S runs one used block
+      // ahead of P.V, so S_X(j+1) overlaps the softmax of block j.
+      const int x = warp == 1 ? 0 : 1;
+      const bool leader = elect_one();
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
+      const uint64_t dq = sdesc_sw128(sQ + x * kTile, 16, 1024);
+      const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sV, kTile, 1024);
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+        return __all_sync(0xffffffffu, ok);
+      };
+      auto wait2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) -> bool {
+        const bool lo = lane < 16;
+        const bool ok = mbar_wait_bounded(smem_u32(lo ? a : b), lo ? pa : pb, abort, kTimeoutNs);
+        return __all_sync(0xffffffffu, ok);
+      };
+      PairSched ss, sp;
+      int bs = 0, jS = 0, jP = 0;
+      // the S cursor: block bs, used by this tile or only released by it
+      auto advance_s = [&]() -> bool {
+        ss.next(g.n_depth, g.nb);
+        const bool use = g.uses(x, ss, p.L);
+        const int st = bs % kNS;
+        const bool ok = (use && jS >= 1)
+                            ? wait2(&bars->k_full[st], (bs / kNS) & 1, &bars->s_free[x], (jS - 1) & 1)
+                            : wait(&bars->k_full[st], (bs / kNS) & 1);
+        if (!ok) return false;
+        tc_fence_after();
+        if (use) {
+          if (leader) {
+            const uint64_t dks = dk + (uint64_t)((st * kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tbase + kColS + x * 128, dq + (uint64_t)(kk * 2), dks + (uint64_t)(kk * 2), idS,
+                     kk > 0);
+            tc_commit(smem_u32(&bars->k_empty[st]));
+            tc_commit(smem_u32(&bars->s_full[x]));
+          }
+          ++jS;
+        } else if (leader) {
+          mbar_arrive(smem_u32(&bars->k_empty[st]));
+        }
+        __syncwarp();
+        ++bs;
+        return true;
+      };
+      bool ok = wait(&bars->q_full, 0);
+      while (ok && bs < g.nb && jS < 1) ok = advance_s();
+      for (int bp = 0; ok && bp < g.nb; ++bp) {
+        sp.next(g.n_depth, g.nb);
+        const bool use = g.uses(x, sp, p.L);
+        const int st = bp % kNS;
+        if (use) {
+          while (ok && bs < g.nb && jS < jP + 2) ok = advance_s();
+          if (!ok) break;
+          if (!wait2(&bars->p_full[x], jP & 1, &bars->v_full[st], (bp / kNS) & 1)) break;
+          tc_fence_after();
+          if (leader) {
+            const uint64_t dvs = dv + (uint64_t)((st * kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tbase + kColO + x * 64, tbase + kColP + x * 64 + kk * 8,
+                     dvs + (uint64_t)((kk * 2048) >> 4), idPV, (jP > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(&bars->v_empty[st]));
+            tc_commit(smem_u32(&bars->pv_done[x]));
+          }
+          __syncwarp();
+          ++jP;
+        } else {
+          if (!wait(&bars->v_full[st], (bp / kNS) & 1)) break;
+          if (leader) mbar_arrive(smem_u32(&bars->v_empty[st]));
+          __syncwarp();
+        }
+      }
+      while (ok && bs < g.nb) ok = advance_s();  // release the remaining K stages
+      if (leader) {
+        int never = 0;
+        tc_commit(smem_u32(&bars->mma_done[x]));
+        mbar_wait_bounded(smem_u32(&bars->mma_done[x]), 0, &never, kTimeoutNs);
+      }
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+    // ---------------------------------------------------- softmax + epilogue
+    const int tx = (warp - 4) >> 2;  // tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
+    const int p0x = g.p0 + tx * g.P;
+    const int lp = row >> p.lgG;
+    const int t_row = p0x + lp;
+    const int h_row = hk * G + (row & (G - 1));
+    const bool valid = lp < g.npos[tx];
+    const int t_mask = min(t_row, p.T - 1);
+    const int d_lo = (tx * g.P + lp) * p.L;      // pair-relative depth rows of this row
+    const int d_hi = valid ? d_lo + p.L : d_lo;  // rows past T keep no depth column
+    const float sl = p.scale_log2;
+    const uint32_t colS = kColS + tx * 128, colO = kColO + tx * 64, colP = kColP + tx * 64;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = g.npos[tx] > 0;
+    int j = 0;  // blocks of this tile so far
+    PairSched sch;
+    for (int b = 0; ok && b < g.nb; ++b) {
+      sch.next(g.n_depth, g.nb);
+      if (!g.uses(tx, sch, p.L)) continue;
+      if (!warp_wait(smem_u32(&bars->s_full[tx]), j & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, colS + c * 32), x + c * 32);
+      tmem_ld_wait();
+      // S is in registers: the tile's S columns may take its next block
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->s_free[tx]));
+      {
+        int lo = 0, hi = BN;
+        if (sch.depth) {
+          lo = d_lo - sch.index * BN;
+          hi = d_hi - sch.index * BN;
+        } else {
+          const int k0 = sch.index * BN;
+          if (k0 + BN - 1 > p0x) hi = t_mask - k0 + 1;
+        }
+        lo = max(lo, 0);
+        hi = min(hi, BN);
+        if (lo > 0 || hi < BN) {
+          const unsigned span = (unsigned)max(hi - lo, 0);
+#pragma unroll
+          for (int c = 0; c < BN; ++c) x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;
+        }
+      }
+      float mx;
+      {
+        float a1[43];
+#pragma unroll
+        for (int i = 0; i < 42; ++i)
+          a1[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]),
+                        __uint_as_float(x[3 * i + 2]));
+        a1[42] = fmaxf(__uint_as_float(x[126]), __uint_as_float(x[127]));
+        float a2[15];
+#pragma unroll
+        for (int i = 0; i < 14; ++i) a2[i] = max3f(a1[3 * i], a1[3 * i + 1], a1[3 * i + 2]);
+        a2[14] = a1[42];
+        float a3[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
+        mx = fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
+      }
+      uint32_t pk[BN / 2];
+      auto compute_p = [&](float m) -> float {
+        const float nbase = (m == -INFINITY) ? 0.f : -m;
+        const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
+        uint64_t acc[8];
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          float u, w;
+          f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2), u, w);
+          const float e0 = ex2_approx(u), e1 = ex2_approx(w);
+          pk[c] = pack_bf16x2(e0, e1);
+          acc[c & 7] = c < 8 ? f2(e0, e1) : fadd2(acc[c & 7], f2(e0, e1));
+        }
+        acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+        acc[4] = fadd2(fadd2(acc[4], acc[5]), fadd2(acc[6], acc[7]));
+        acc[0] = fadd2(acc[0], acc[4]);
+        float u, w;
+        f2_split(acc[0], u, w);
+        return u + w;
+      };
+      // stale-reference fast path, max-first slow path with a lazy rescale of
+      // O and l (as in the d = 128 kernel)
+      float sum = 0.f;
+      bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+      if (!slow) {
+        sum = compute_p(m_ref);
+        slow = __any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold);
+      }
+      if (slow) {
+        const bool need = mx > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mx : m_ref;
+          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+          if (j > 0) {
+            if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              const uint32_t ta = tmem_addr(tbase, lane_base, colO + c * 32);
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(ta, r);
+            }
+            tmem_st_wait();
+          }
+          l *= alpha;
+          m_ref = m_new;
+        }
+        sum = compute_p(m_ref);
+      }
+      l += sum;
+      // the tile's P columns hold P of its previous block until that P.V is done
+      if (j >= 1) {
+        if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(tmem_addr(tbase, lane_base, colP + c * 32), pk + c * 32);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->p_full[tx]));
+      ++j;
+    }
+    if (ok && j > 0) ok = warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort);
+    if (ok && j > 0) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, colO + c * 32), r);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+  if (tid == 0 && bars->abort) atomicCAS(p.err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d != D) return cudaErrorInvalidValue;
+  const int lgG = __builtin_ctz((unsigned)a.G);
+  const int P = BM >> lgG;
+  const int ntiles = (a.T + P - 1) / P;
+  const int npairs = (ntiles + 1) / 2;
+  CUtensorMap tq, tk, tv, tkd, tvd;
+  const uint64_t row = (uint64_t)D * 2;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hq};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)P};
+    if (encode_bf16_sw128(&tq, a.q, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hk};
+    const uint32_t box[3] = {64, 1, BN};
+    if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  if (a.L > 0) {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
+    const uint64_t str[1] = {row};
+    const uint32_t box[2] = {64, BN};
+    if (encode_bf16_sw128(&tkd, a.kd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  } else {
+    tkd = tk;  // never read when L == 0
+    tvd = tv;
+  }
+  PpParams prm;
+  prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.npairs = npairs;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.o = (__nv_bfloat16*)a.o;
+  prm.lse = a.lse;
+  prm.err = a.err;
+  cudaError_t e = cudaFuncSetAttribute(moda_fwd_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  moda_fwd_pp_kernel<<<(unsigned)((int64_t)npairs * a.Hk), kThreads, kSmemBytes, stream>>>(
+      tq, tk, tv, tkd, tvd, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace moda

@@ -588,7 +588,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
-  return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
+  return a.d == 128 ? launch_d<128>(a, stream) : launch_fwd_pp(a, stream);
 }
 
 }  // namespace moda

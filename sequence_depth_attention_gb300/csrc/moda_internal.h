@@ -72,6 +72,8 @@ cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
+// d = 64: two query tiles per CTA in ping-pong.
+cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream);
 // Depth part on CUDA cores, merged into o and lse that hold the L = 0 result.
 cudaError_t launch_fwd_depth_cc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
