@@ -16,7 +16,8 @@
 // lane). TMEM: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384),
 // P_A [384,448), P_B [448,512). Each issuer runs its S stream one used block
 // ahead of its P.V stream: S_X(j+1) once the softmax holds S_X(j) in
-// registers, P_X(j).V(j) once P_X(j) is stored.
+// registers, P_X(j).V(j) once P_X(j) is stored (the S cursor runs at most
+// two blocks ahead of the P.V cursor).
 // A block may be used by A, B or both (the last sequence block, and the
 // depth blocks, which hold one tile's positions or both). Every K/V stage is
 // released by two arrivals per block, one per tile: the MMA commit of a tile
@@ -269,15 +270,19 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         ++bs;
         return true;
       };
+      // The S cursor stays at most two blocks ahead of the P.V cursor: S of
+      // block bp+1 (when this tile uses it) goes out before P.V of block bp,
+      // and no cursor ever waits for a block the rings cannot hold yet (a tile
+      // whose next used block lies far ahead would otherwise hold back the
+      // stages the other tile needs).
       bool ok = wait(&bars->q_full, 0);
-      while (ok && bs < g.nb && jS < 1) ok = advance_s();
       for (int bp = 0; ok && bp < g.nb; ++bp) {
+        while (ok && bs < g.nb && bs <= bp + 1) ok = advance_s();
+        if (!ok) break;
         sp.next(g.n_depth, g.nb);
         const bool use = g.uses(x, sp, p.L);
         const int st = bp % kNS;
         if (use) {
-          while (ok && bs < g.nb && jS < jP + 2) ok = advance_s();
-          if (!ok) break;
           if (!wait2(&bars->p_full[x], jP & 1, &bars->v_full[st], (bp / kNS) & 1)) break;
           tc_fence_after();
           if (leader) {

@@ -70,6 +70,13 @@ EDGE = [
     Workload("T300-G16-L48", T=300, Hq=16, Hk=1, d=64, L=48),
     Workload("T513-G4-L0", T=513, Hq=8, Hk=2, d=128, L=0),
     Workload("T1000-G4-L24", T=1000, Hq=8, Hk=2, d=128, L=24, seed=4),
+    # d = 64 runs two tiles per CTA: pairs whose tiles use very different
+    # K/V blocks (long depth runs of one tile), odd tile counts, a lone tile
+    Workload("T200-G1-L33-d64", T=200, Hq=3, Hk=3, d=64, L=33),
+    Workload("T385-G4-L46-d64", T=385, Hq=8, Hk=2, d=64, L=46, seed=11),
+    Workload("T700-G2-L90-d64", T=700, Hq=4, Hk=2, d=64, L=90, seed=12),
+    Workload("T1000-G8-L64-d64", T=1000, Hq=16, Hk=2, d=64, L=64, seed=13),
+    Workload("T100-G1-L200-d64", T=100, Hq=2, Hk=2, d=64, L=200, seed=14),
 ]
 
 
