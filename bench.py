@@ -397,6 +397,87 @@ def main(argv=None):
         "clocks": clk,
     }
 
+    # ---- end to end: pinned host inputs in, o and lse out, every step ----
+    # (measured right after the device-resident timing, before the other
+    # phases' allocations can change the host link's behaviour)
+    if not args.no_e2e:
+        hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hkd, hvd = (t.cpu().pin_memory() for t in (kd_raw, vd_raw))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        # Double-buffered device inputs: the copy engines move step i+1's
+        # inputs (every byte of them, from pinned host memory) while step i
+        # packs and runs on the compute stream; the host link is the bound.
+        copy = torch.cuda.Stream(device=dev)
+        sets = [(q, k, v, kd_raw, vd_raw)]
+        sets.append(tuple(torch.empty_like(t) for t in sets[0]))
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        for ev in consumed:
+            ev.record(stream)
+        n_issued = [0]
+
+        def issue_copy(i):
+            dq, dk, dv, dkr, dvr = sets[i % 2]
+            copy.wait_event(consumed[i % 2])  # the set's previous step is done with it
+            with torch.cuda.stream(copy):
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk_, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                if w.L:
+                    dkr.copy_(hkd, non_blocking=True)
+                    dvr.copy_(hvd, non_blocking=True)
+                copied[i % 2].record(copy)
+
+        def e2e_step(n):
+            """Step i of n: waits for its inputs, starts step i+1's copy (unless
+            it is the last), then packs, runs and reads back."""
+            i = n_issued[0]
+            n_issued[0] += 1
+            if i == 0:
+                issue_copy(0)
+            stream.wait_event(copied[i % 2])
+            if i + 1 < n:
+                issue_copy(i + 1)  # overlaps this step's compute
+            dq, dk, dv, dkr, dvr = sets[i % 2]
+            if w.L:
+                moda.moda_pack_depth(dkr, kd, stream=stream)
+                moda.moda_pack_depth(dvr, vd, stream=stream)
+            moda.moda_fwd(dq, dk, dv, kd if w.L else None, vd if w.L else None, w.scale, o=o,
+                          lse=lse, stream=stream)
+            consumed[i % 2].record(stream)
+            with torch.cuda.stream(stream):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+
+        for _ in range(W):
+            e2e_step(W)
+        torch.cuda.synchronize(dev)
+        n_issued[0] = 0
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            e2e_step(K)
+        b.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / K, dist, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv)) + \
+            (sum(t.numel() * t.element_size() for t in (hkd, hvd)) if w.L else 0)
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        line["e2e"] = {"value": job_tflops(F, e2e_ms, world), "unit": "TFLOP/s",
+                       "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h,
+                       "transfer": "every step's q, k, v, kd, vd copied from pinned host memory by "
+                                   "the copy engines into one of two device input sets, overlapping "
+                                   "the previous step's pack + forward; o, lse copied back each step; "
+                                   "the timed region runs from the first step's copy to the last "
+                                   "step's read-back"}
+        host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}
+        del sets  # the second device input set
+    else:
+        host = None
+
     # ---- the depth variant choice: CUDA-core depth in a second pass ----
     if w.L and args.variant_steps > 0:
         moda.moda_fwd(q, k, v, kd, vd, w.scale, o=o, lse=lse, stream=stream,
@@ -541,84 +622,6 @@ def main(argv=None):
                            "flops_counted": Fp,
                            "unfused_cublas_gemm_plus_slot_write_ms": ums}
         del xp, wk, wv
-
-    # ---- end to end: pinned host inputs in, o and lse out, every step ----
-    if not args.no_e2e:
-        hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
-        hkd, hvd = (t.cpu().pin_memory() for t in (kd_raw, vd_raw))
-        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        # Double-buffered device inputs: the copy engines move step i+1's
-        # inputs (every byte of them, from pinned host memory) while step i
-        # packs and runs on the compute stream; the host link is the bound.
-        copy = torch.cuda.Stream(device=dev)
-        sets = [(q, k, v, kd_raw, vd_raw)]
-        sets.append(tuple(torch.empty_like(t) for t in sets[0]))
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-        consumed = [torch.cuda.Event(), torch.cuda.Event()]
-        for ev in consumed:
-            ev.record(stream)
-        n_issued = [0]
-
-        def issue_copy(i):
-            dq, dk, dv, dkr, dvr = sets[i % 2]
-            copy.wait_event(consumed[i % 2])  # the set's previous step is done with it
-            with torch.cuda.stream(copy):
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk_, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                if w.L:
-                    dkr.copy_(hkd, non_blocking=True)
-                    dvr.copy_(hvd, non_blocking=True)
-                copied[i % 2].record(copy)
-
-        def e2e_step(n):
-            """Step i of n: waits for its inputs, starts step i+1's copy (unless
-            it is the last), then packs, runs and reads back."""
-            i = n_issued[0]
-            n_issued[0] += 1
-            if i == 0:
-                issue_copy(0)
-            stream.wait_event(copied[i % 2])
-            if i + 1 < n:
-                issue_copy(i + 1)  # overlaps this step's compute
-            dq, dk, dv, dkr, dvr = sets[i % 2]
-            if w.L:
-                moda.moda_pack_depth(dkr, kd, stream=stream)
-                moda.moda_pack_depth(dvr, vd, stream=stream)
-            moda.moda_fwd(dq, dk, dv, kd if w.L else None, vd if w.L else None, w.scale, o=o,
-                          lse=lse, stream=stream)
-            consumed[i % 2].record(stream)
-            with torch.cuda.stream(stream):
-                ho.copy_(o, non_blocking=True)
-                hl.copy_(lse, non_blocking=True)
-
-        for _ in range(W):
-            e2e_step(W)
-        torch.cuda.synchronize(dev)
-        n_issued[0] = 0
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(K):
-            e2e_step(K)
-        b.record(stream)
-        barrier()
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / K, dist, dev)
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv)) + \
-            (sum(t.numel() * t.element_size() for t in (hkd, hvd)) if w.L else 0)
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        line["e2e"] = {"value": job_tflops(F, e2e_ms, world), "unit": "TFLOP/s",
-                       "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h,
-                       "transfer": "every step's q, k, v, kd, vd copied from pinned host memory by "
-                                   "the copy engines into one of two device input sets, overlapping "
-                                   "the previous step's pack + forward; o, lse copied back each step; "
-                                   "the timed region runs from the first step's copy to the last "
-                                   "step's read-back"}
-        host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}
-    else:
-        host = None
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if host is None:
