@@ -1,5 +1,6 @@
 // MoDA forward on the 5th-generation tensor core (sm_103a): TMA-staged tiles,
-// tcgen05.mma into tensor memory (TMEM), warp-specialised pipeline.
+// tcgen05.mma into tensor memory (TMEM), warp-specialised pipeline. This
+// kernel serves d = 128; d = 64 runs two tiles per CTA (fwd_pp.cu).
 //
 // What it computes is Mixture-of-Depths Attention, Sec. 2.2 (one softmax over
 // the causal sequence keys of the layer and the L depth slots of the same
@@ -67,8 +68,9 @@ template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;     // 64-column (128-byte) swizzle boxes per row
   static constexpr int kBoxBytes = 128 * 64 * 2;
-  static constexpr int kNSK = D == 128 ? 3 : 5;  // K stages in the K region
-  static constexpr int kNSV = D == 128 ? 3 : 6;  // V stages
+  static_assert(D == 128, "d = 64 runs the two-tile kernel (fwd_pp.cu)");
+  static constexpr int kNSK = 3;  // K stages in the K region
+  static constexpr int kNSV = 3;  // V stages
   // one more K stage lives in the Q region once Q has been copied to TMEM
   static constexpr int kNSKT = kNSK + 1;
   static constexpr int kQBytes = BM * D * 2;
@@ -587,6 +589,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+// d = 128 runs this kernel; d = 64 the two-tiles-per-CTA kernel of fwd_pp.cu.
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   return a.d == 128 ? launch_d<128>(a, stream) : launch_fwd_pp(a, stream);
 }
