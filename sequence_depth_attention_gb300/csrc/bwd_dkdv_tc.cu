@@ -14,9 +14,10 @@
 //
 // Roles (12 warps): warp 0 TMA (K, V once, then the Q/dO ring); warp 1 issues
 // MMAs; warps 4-7 and 8-11 each take 32 of the 64 columns for all 128 keys.
-// TMEM columns: S^T [0,64), dP^T [64,128), two P^T|dS^T buffers [128,192)
-// [192,256) (per column half: 16 columns of P^T then 16 of dS^T, bf16 pairs),
-// dV [256,256+d), dK [256+d,256+2d).
+// TMEM columns: S^T [0,64), dP^T [64,128), P^T|dS^T [128,192) (per column
+// half: 16 columns of P^T then 16 of dS^T, bf16 pairs), K [192,192+d/2) (bf16
+// pairs, copied once: the A operand of S^T, so those N = 64 MMAs read only the
+// Q sub-tile from shared memory), dV [256,256+d), dK [256+d,256+2d).
 // Issue order: S_0 dP_0, then per c: S_{c+1} dP_{c+1} once the softmax holds
 // S_c and dP_c in registers, then dV_c dK_c once P^T_c and dS^T_c are stored.
 // All waits are bounded; on expiry the CTA drains and latches MODA_ERR_TIMEOUT.
@@ -51,7 +52,8 @@ struct KvCfg {
   static constexpr int kOffRow = kOffQ + kNS * 2 * kQTile;  // per-warp lse2 / D staging
   static constexpr int kOffBar = kOffRow + 8 * 2 * 32 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr uint32_t kColS = 0, kColP = 64, kColB = 128, kColV = 256, kColK = 256 + D;
+  static constexpr uint32_t kColS = 0, kColP = 64, kColB = 128, kColKt = 192, kColV = 256,
+                            kColK = 256 + D;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -60,6 +62,7 @@ struct alignas(8) KvBars {
   uint64_t q_full[6], q_empty[6];
   uint64_t s_full, s_free;
   uint64_t pd_full[2], pd_done[2];
+  uint64_t k_tmem;  // the block's K rows are in TMEM
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -149,6 +152,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(smem_u32(&bars->pd_done[b]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
+    mbar_init(smem_u32(&bars->k_tmem), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -217,9 +221,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
           const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + C::kColS, dk_ + ka, dq_ + stage + qa, idS, kk > 0);
+          mma_ts(tbase + C::kColS, tbase + C::kColKt + kk * 8, dq_ + stage + qa, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -235,7 +238,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const int s = i % C::kNS, b = i & 1;
       const uint32_t stage = (uint32_t)(s * 2 * C::kQTile) >> 4;
       if (leader) {
-        const uint32_t abuf = tbase + C::kColB + b * 64;
+        const uint32_t abuf = tbase + C::kColB;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acol = abuf + (kk >> 1) * 32 + (kk & 1) * 8;
@@ -249,7 +252,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       __syncwarp();
     };
-    bool ok = wait(&bars->kv_full, 0) && wait(&bars->q_full[0], 0);
+    bool ok = wait(&bars->kv_full, 0) && wait(&bars->k_tmem, 0) && wait(&bars->q_full[0], 0);
     if (ok) {
       tc_fence_after();
       issue_sdp(0);
@@ -277,6 +280,28 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int row = q4 * 32 + lane;  // key within the block
     const uint32_t lane_base = (uint32_t)q4 * 32;
     const int key = q0 + row;
+    // K row -> TMEM columns [kColKt, kColKt + d/2) as bf16 pairs in row order,
+    // the A operand of S^T = K Q^T for every sub-tile (so those MMAs read only
+    // the 64-row Q sub-tile from shared memory); the first half's warps copy it
+    if (half == 0) {
+      bool kok = warp_wait(smem_u32(&bars->kv_full), 0, abort);
+      if (kok) {
+        const uint8_t* krow = smem + C::kOffK + row * 128;
+#pragma unroll
+        for (int c = 0; c < C::kBoxes; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(krow + c * C::kKBox + ((k ^ (row & 7)) << 4));
+            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+          }
+          tmem_st32(tmem_addr(tbase, lane_base, C::kColKt + c * 32), w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->k_tmem));
+      }
+    }
     float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64;
     const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
     const int col = half * 32 + lane;  // the column this lane fetches lse and D for
@@ -314,15 +339,15 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       } else {
         pds_pack<false>(x, y, rowbuf, sl2, 0, pk);
       }
-      // buffer i&1 last held sub-tile i-2: the tensor core must have consumed it
-      if (i >= 2) {
-        if (!warp_wait(smem_u32(&bars->pd_done[i & 1]), ((i - 2) >> 1) & 1, abort)) {
+      // the P^T|dS^T columns hold sub-tile i-1's until its dV, dK are done
+      if (i >= 1) {
+        if (!warp_wait(smem_u32(&bars->pd_done[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
-      tmem_st32(tmem_addr(tbase, lane_base, C::kColB + (i & 1) * 64 + half * 32), pk);
+      tmem_st32(tmem_addr(tbase, lane_base, C::kColB + half * 32), pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->pd_full[i & 1]));
