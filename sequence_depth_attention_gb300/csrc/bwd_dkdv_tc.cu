@@ -14,12 +14,16 @@
 //
 // Roles (12 warps): warp 0 TMA (K, V once, then the Q/dO ring); warp 1 issues
 // MMAs; warps 4-7 and 8-11 each take 32 of the 64 columns for all 128 keys.
-// TMEM columns: S^T [0,64), dP^T [64,128), P^T|dS^T [128,192) (per column
-// half: 16 columns of P^T then 16 of dS^T, bf16 pairs), K [192,192+d/2) (bf16
+// TMEM columns: two buffers b of S^T [128b,128b+64) and dP^T [128b+64,128b+128),
+// sub-tile c in buffer c&1; the elementwise warps write P^T|dS^T over the S^T
+// columns they read (per column half: 16 columns of P^T then 16 of dS^T, bf16
+// pairs); dV [256,256+d), dK [256+d,256+2d); for d = 64 also K [384,416) (bf16
 // pairs, copied once: the A operand of S^T, so those N = 64 MMAs read only the
-// Q sub-tile from shared memory), dV [256,256+d), dK [256+d,256+2d).
-// Issue order: S_0 dP_0, then per c: S_{c+1} dP_{c+1} once the softmax holds
-// S_c and dP_c in registers, then dV_c dK_c once P^T_c and dS^T_c are stored.
+// Q sub-tile from shared memory).
+// Issue order: dP_0 S_0 dP_1 S_1, then per c: dV_c dK_c once P^T_c and dS^T_c
+// are stored, dP_{c+2} (its columns were free once the elementwise warps read
+// dP_c), and S_{c+2} once dV_c and dK_c have read buffer c&1. The tensor core
+// works on one sub-tile while the elementwise warps work on the next.
 // All waits are bounded; on expiry the CTA drains and latches MODA_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -52,17 +56,18 @@ struct KvCfg {
   static constexpr int kOffRow = kOffQ + kNS * 2 * kQTile;  // per-warp lse2 / D staging
   static constexpr int kOffBar = kOffRow + 8 * 2 * 32 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr uint32_t kColS = 0, kColP = 64, kColB = 128, kColKt = 192, kColV = 256,
-                            kColK = 256 + D;
+  static constexpr bool kKInTmem = D == 64;  // with d = 128, dV and dK fill the rest of TMEM
+  static constexpr uint32_t kColS = 0, kColP = 64, kColBuf = 128, kColV = 256, kColK = 256 + D,
+                            kColKt = 256 + 2 * D;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct alignas(8) KvBars {
   uint64_t kv_full;
   uint64_t q_full[6], q_empty[6];
-  uint64_t s_full, s_free;
-  uint64_t pd_full[2], pd_done[2];
-  uint64_t k_tmem;  // the block's K rows are in TMEM
+  uint64_t s_full[2];               // S^T, dP^T of buffer b computed
+  uint64_t pd_full[2], pd_done[2];  // P^T|dS^T of buffer b stored / consumed
+  uint64_t k_tmem;                  // the block's K rows are in TMEM (d = 64)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -145,9 +150,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(smem_u32(&bars->q_full[s]), 1);
       mbar_init(smem_u32(&bars->q_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->s_free), 256);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
       mbar_init(smem_u32(&bars->pd_full[b]), 256);
       mbar_init(smem_u32(&bars->pd_done[b]), 1);
     }
@@ -206,69 +210,84 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    const bool leader = elect_one();
-    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, false);  // S^T, dP^T: K-major A and B
-    constexpr uint32_t idG = idesc_bf16_f32(BK, D, true);    // dV, dK: B read MN-major
-    const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
-    const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t dqmn = sdesc_sw128(sQ, C::kQBox, 1024);
-    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
-      return __all_sync(0xffffffffu, ok);
-    };
-    auto issue_sdp = [&](int i) {  // S^T_i and dP^T_i
-      const uint32_t stage = (uint32_t)((i % C::kNS) * 2 * C::kQTile) >> 4;
-      if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
-          mma_ts(tbase + C::kColS, tbase + C::kColKt + kk * 8, dq_ + stage + qa, idS, kk > 0);
-        }
+    // One thread runs the whole schedule, waits included: the tensor core
+    // queues few MMAs, so every instruction on this thread between two MMAs
+    // can leave it idle, and the elementwise warps share its issue slots.
+    if (elect_one()) {
+      constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, false);  // S^T, dP^T: K-major A and B
+      constexpr uint32_t idG = idesc_bf16_f32(BK, D, true);    // dV, dK: B read MN-major
+      // every descriptor here has the same high word (SBO 1024, 128-byte
+      // swizzle); tile offsets are 32-bit adds to the start address field
+      const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024);
+      const uint32_t hi = (uint32_t)(dq_ >> 32), q_lo = (uint32_t)dq_;
+      const uint32_t k_lo = (uint32_t)sdesc_sw128(sK, 16, 1024), v_lo = (uint32_t)sdesc_sw128(sV, 16, 1024);
+      const uint32_t qmn_lo = (uint32_t)sdesc_sw128(sQ, C::kQBox, 1024);
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+      };
+      auto stage_of = [&](int i) { return (uint32_t)((i % C::kNS) * 2 * C::kQTile) >> 4; };
+      auto issue_dp = [&](int i) {  // dP^T_i = V dO_i^T into buffer i&1
+        const uint32_t qs = q_lo + stage_of(i) + (C::kQTile >> 4);
+        const uint32_t acc = tbase + (i & 1) * C::kColBuf + C::kColP;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
-          const uint32_t qa = ((C::kQTile + (kk >> 2) * C::kQBox + (kk & 3) * 32)) >> 4;
-          mma_ss(tbase + C::kColP, dv_ + ka, dq_ + stage + qa, idS, kk > 0);
+          const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
+          mma_ss(acc, desc_join(v_lo + ka, hi), desc_join(qs + qa, hi), idS, kk > 0);
         }
-        tc_commit(smem_u32(&bars->s_full));
-      }
-      __syncwarp();
-    };
-    auto issue_grad = [&](int i) {  // dV += P^T_i dO_i, dK += dS^T_i Q_i; frees stage and buffer
-      const int s = i % C::kNS, b = i & 1;
-      const uint32_t stage = (uint32_t)(s * 2 * C::kQTile) >> 4;
-      if (leader) {
-        const uint32_t abuf = tbase + C::kColB;
+      };
+      auto issue_s = [&](int i) {  // S^T_i = K Q_i^T into buffer i&1; buffer i&1 is then complete
+        const uint32_t qs = q_lo + stage_of(i);
+        const uint32_t acc = tbase + (i & 1) * C::kColBuf + C::kColS;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
+          const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
+          if constexpr (C::kKInTmem)
+            mma_ts(acc, tbase + C::kColKt + kk * 8, desc_join(qs + qa, hi), idS, kk > 0);
+          else
+            mma_ss(acc, desc_join(k_lo + ka, hi), desc_join(qs + qa, hi), idS, kk > 0);
+        }
+        tc_commit(smem_u32(&bars->s_full[i & 1]));
+      };
+      auto issue_grad = [&](int i) {  // dV += P^T_i dO_i, dK += dS^T_i Q_i; frees stage and buffer
+        const int s = i % C::kNS, b = i & 1;
+        const uint32_t qs = qmn_lo + stage_of(i);
+        const uint32_t abuf = tbase + b * C::kColBuf + C::kColS;
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acol = abuf + (kk >> 1) * 32 + (kk & 1) * 8;
-          const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
-          mma_ts(tbase + C::kColV, acol, dqmn + stage + (C::kQTile >> 4) + boff, idG,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tbase + C::kColK, acol + 16, dqmn + stage + boff, idG, (i > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t boff = (uint32_t)(kk * 2048) >> 4;
+          mma_ts(tbase + C::kColV, acol, desc_join(qs + (C::kQTile >> 4) + boff, hi), idG, kk > 0 ? 1u : acc0);
+          mma_ts(tbase + C::kColK, acol + 16, desc_join(qs + boff, hi), idG, kk > 0 ? 1u : acc0);
         }
         tc_commit(smem_u32(&bars->q_empty[s]));
         tc_commit(smem_u32(&bars->pd_done[b]));
+      };
+      bool ok = wait(&bars->kv_full, 0) && (!C::kKInTmem || wait(&bars->k_tmem, 0));
+      for (int i = 0; ok && i < n && i < 2; ++i) {
+        ok = wait(&bars->q_full[i], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(i);
+          issue_s(i);
+        }
       }
-      __syncwarp();
-    };
-    bool ok = wait(&bars->kv_full, 0) && wait(&bars->k_tmem, 0) && wait(&bars->q_full[0], 0);
-    if (ok) {
-      tc_fence_after();
-      issue_sdp(0);
-    }
-    for (int i = 0; ok && i < n; ++i) {
-      if (i + 1 < n) {
-        if (!wait(&bars->s_free, i & 1)) break;
-        if (!wait(&bars->q_full[(i + 1) % C::kNS], ((i + 1) / C::kNS) & 1)) break;
+      for (int i = 0; ok && i < n; ++i) {
+        if (!wait(&bars->pd_full[i & 1], (i >> 1) & 1)) break;
         tc_fence_after();
-        issue_sdp(i + 1);
+        issue_grad(i);
+        if (i + 2 < n) {
+          if (!wait(&bars->q_full[(i + 2) % C::kNS], ((i + 2) / C::kNS) & 1)) break;
+          tc_fence_after();
+          issue_dp(i + 2);
+          // S^T_{i+2} overwrites the P^T|dS^T columns that dV_i and dK_i read
+          if (!wait(&bars->pd_done[i & 1], (i >> 1) & 1)) break;
+          tc_fence_after();
+          issue_s(i + 2);
+        }
       }
-      if (!wait(&bars->pd_full[i & 1], (i >> 1) & 1)) break;
-      tc_fence_after();
-      issue_grad(i);
-    }
-    if (leader) {
       int never = 0;
       tc_commit(smem_u32(&bars->mma_done));
       mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);
@@ -283,7 +302,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // K row -> TMEM columns [kColKt, kColKt + d/2) as bf16 pairs in row order,
     // the A operand of S^T = K Q^T for every sub-tile (so those MMAs read only
     // the 64-row Q sub-tile from shared memory); the first half's warps copy it
-    if (half == 0) {
+    if (C::kKInTmem && half == 0) {
       bool kok = warp_wait(smem_u32(&bars->kv_full), 0, abort);
       if (kok) {
         const uint8_t* krow = smem + C::kOffK + row * 128;
@@ -319,17 +338,16 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         rowbuf[32 + lane] = dd;
         __syncwarp();
       }
-      if (!warp_wait(smem_u32(&bars->s_full), i & 1, abort)) {
+      const uint32_t buf = (i & 1) * C::kColBuf;
+      if (!warp_wait(smem_u32(&bars->s_full[i & 1]), (i >> 1) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t x[32], y[32];
-      tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + half * 32), x);
-      tmem_ld32(tmem_addr(tbase, lane_base, C::kColP + half * 32), y);
+      tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColS + half * 32), x);
+      tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColP + half * 32), y);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free));
       // causal: column c (position t0 + c/G) sees this key iff key <= position;
       // sub-tiles at or after the block's last key need no mask
       uint32_t pk[32];
@@ -339,15 +357,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       } else {
         pds_pack<false>(x, y, rowbuf, sl2, 0, pk);
       }
-      // the P^T|dS^T columns hold sub-tile i-1's until its dV, dK are done
-      if (i >= 1) {
-        if (!warp_wait(smem_u32(&bars->pd_done[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      tmem_st32(tmem_addr(tbase, lane_base, C::kColB + half * 32), pk);
+      // in place over the S^T columns this thread has just read
+      tmem_st32(tmem_addr(tbase, lane_base, buf + C::kColS + half * 32), pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->pd_full[i & 1]));

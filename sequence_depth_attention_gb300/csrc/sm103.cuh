@@ -173,6 +173,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// A descriptor from its two words. The low word holds the start address
+// field (bits 0-13, address >> 4) and the leading byte offset; a tile offset
+// below 256 KB is a plain 32-bit add on it.
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A and B and an fp32 accumulator.
 //   bits 4-5 D type (1 = f32), 7-9 A type (1 = bf16), 10-12 B type (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (1 = MN), bits 17-22 N >> 3,
