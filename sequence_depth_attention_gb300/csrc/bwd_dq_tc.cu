@@ -190,75 +190,69 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    const bool leader = elect_one();
-    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);  // S, dP: K-major A and B
-    constexpr uint32_t idQ = idesc_bf16_f32(BM, D, true);    // dQ: B = K read MN-major
-    const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024), do_ = sdesc_sw128(sO, 16, 1024);
-    const uint64_t dk = sdesc_sw128(sK, 16, 1024), dv = sdesc_sw128(sV, 16, 1024);
-    const uint64_t dkmn = sdesc_sw128(sK, C::kBoxBytes, 1024);
-    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool ok = mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
-      return __all_sync(0xffffffffu, ok);
-    };
-    auto wait2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) -> bool {
-      const bool lo = lane < 16;
-      const bool ok = mbar_wait_bounded(smem_u32(lo ? a : b), lo ? pa : pb, abort, kTimeoutNs);
-      return __all_sync(0xffffffffu, ok);
-    };
-    auto issue_sdp = [&](int j) {  // S_j and dP_j; frees V_j when done
-      const int ks = j % C::kNSK, vs = j % C::kNSV;
-      if (leader) {
-        const uint64_t dks = dk + (uint64_t)((ks * C::kTileBytes) >> 4);
-        const uint64_t dvs = dv + (uint64_t)((vs * C::kTileBytes) >> 4);
+    // One thread runs the whole schedule, waits included: the tensor core
+    // queues few MMAs, so every instruction on this thread between two MMAs
+    // can leave it idle, and the elementwise warps share its issue slots.
+    if (elect_one()) {
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);  // S, dP: K-major A and B
+      constexpr uint32_t idQ = idesc_bf16_f32(BM, D, true);    // dQ: B = K read MN-major
+      // every descriptor here has the same high word (SBO 1024, 128-byte
+      // swizzle); tile offsets are 32-bit adds to the start address field
+      const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024);
+      const uint32_t hi = (uint32_t)(dq_ >> 32), q_lo = (uint32_t)dq_;
+      const uint32_t o_lo = (uint32_t)sdesc_sw128(sO, 16, 1024);
+      const uint32_t k_lo = (uint32_t)sdesc_sw128(sK, 16, 1024), v_lo = (uint32_t)sdesc_sw128(sV, 16, 1024);
+      const uint32_t kmn_lo = (uint32_t)sdesc_sw128(sK, C::kBoxBytes, 1024);
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+      };
+      auto issue_sdp = [&](int j) {  // S_j and dP_j; frees V_j when done
+        const int ks = j % C::kNSK, vs = j % C::kNSV;
+        const uint32_t kb = k_lo + ((uint32_t)(ks * C::kTileBytes) >> 4);
+        const uint32_t vb = v_lo + ((uint32_t)(vs * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + C::kColS, dq_ + off, dks + off, idS, kk > 0);
+          mma_ss(tbase + C::kColS, desc_join(q_lo + off, hi), desc_join(kb + off, hi), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + C::kColP, do_ + off, dvs + off, idS, kk > 0);
+          mma_ss(tbase + C::kColP, desc_join(o_lo + off, hi), desc_join(vb + off, hi), idS, kk > 0);
         }
         tc_commit(smem_u32(&bars->v_empty[vs]));
         tc_commit(smem_u32(&bars->s_full));
-      }
-      __syncwarp();
-    };
-    auto issue_dq = [&](int j) {  // dQ += dS_j K_j; frees K_j when done
-      const int ks = j % C::kNSK, b = j & 1;
-      if (leader) {
-        const uint64_t dks = dkmn + (uint64_t)((ks * C::kTileBytes) >> 4);
+      };
+      auto issue_dq = [&](int j) {  // dQ += dS_j K_j; frees K_j when done
+        const int ks = j % C::kNSK, b = j & 1;
+        const uint32_t kb = kmn_lo + ((uint32_t)(ks * C::kTileBytes) >> 4);
         const uint32_t acol = tbase + C::kColDS + b * 64;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase + C::kColQ, acol + kk * 8, dks + (uint64_t)((kk * 2048) >> 4), idQ,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::kColQ, acol + kk * 8, desc_join(kb + ((uint32_t)(kk * 2048) >> 4), hi), idQ,
+                 kk > 0 ? 1u : acc0);
         tc_commit(smem_u32(&bars->k_empty[ks]));
         tc_commit(smem_u32(&bars->dq_done[b]));
-      }
-      __syncwarp();
-    };
-    bool ok = wait2(&bars->q_full, 0, &bars->k_full[0], 0) && wait(&bars->v_full[0], 0);
-    if (ok) {
-      tc_fence_after();
-      issue_sdp(0);
-    }
-    for (int j = 0; ok && j < nb; ++j) {
-      if (j + 1 < nb) {
-        // S_{j+1}, dP_{j+1} as soon as the softmax holds S_j, dP_j in registers
-        if (!wait(&bars->s_free, j & 1)) break;
-        if (!wait2(&bars->k_full[(j + 1) % C::kNSK], ((j + 1) / C::kNSK) & 1,
-                   &bars->v_full[(j + 1) % C::kNSV], ((j + 1) / C::kNSV) & 1))
-          break;
+      };
+      bool ok = wait(&bars->q_full, 0) && wait(&bars->k_full[0], 0) && wait(&bars->v_full[0], 0);
+      if (ok) {
         tc_fence_after();
-        issue_sdp(j + 1);
+        issue_sdp(0);
       }
-      if (!wait(&bars->ds_full[j & 1], (j >> 1) & 1)) break;
-      tc_fence_after();
-      issue_dq(j);
-    }
-    if (leader) {
+      for (int j = 0; ok && j < nb; ++j) {
+        if (j + 1 < nb) {
+          // S_{j+1}, dP_{j+1} as soon as the softmax holds S_j, dP_j in registers
+          if (!wait(&bars->s_free, j & 1)) break;
+          if (!wait(&bars->k_full[(j + 1) % C::kNSK], ((j + 1) / C::kNSK) & 1)) break;
+          if (!wait(&bars->v_full[(j + 1) % C::kNSV], ((j + 1) / C::kNSV) & 1)) break;
+          tc_fence_after();
+          issue_sdp(j + 1);
+        }
+        if (!wait(&bars->ds_full[j & 1], (j >> 1) & 1)) break;
+        tc_fence_after();
+        issue_dq(j);
+      }
       int never = 0;
       tc_commit(smem_u32(&bars->mma_done));
       mbar_wait_bounded(smem_u32(&bars->mma_done), 0, &never, kTimeoutNs);

@@ -256,77 +256,68 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // Warp 1 issues the S = Q K^T products, warp 3 the O += P V products.
     // Each waits for its own operands and commits its own MMAs, so the
     // waits and fences of one overlap the other's MMAs on the tensor core.
-    // The whole warp follows the pipeline so descriptors stay warp-uniform;
-    // one elected lane issues tcgen05.mma / tcgen05.commit.
-    const bool leader = elect_one();
-    // Two barriers checked in one round trip: lanes 0-15 poll a, 16-31 poll b.
-    auto wait2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) -> bool {
-      const bool lo = lane < 16;
-      const bool ok = mbar_wait_bounded(smem_u32(lo ? a : b), lo ? pa : pb, abort, kTimeoutNs);
-      return __all_sync(0xffffffffu, ok);
-    };
-    uint64_t* done = warp == 1 ? &bars->mma_done : &bars->mma_done_pv;
-    if (warp == 1) {
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
-      // base descriptor; the start-address field (bits 0-13, 16-byte units)
-      // is advanced by adding byte offsets >> 4
+    // One elected thread of each runs its whole schedule, waits included:
+    // the tensor core queues few MMAs, so every instruction between two
+    // MMAs can leave it idle, and the softmax warps share the issue slots.
+    if (elect_one()) {
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
+      };
+      // all descriptors here share the high word (SBO 1024, 128-byte swizzle);
+      // tile offsets are 32-bit adds to the start address field of the low word
       const uint64_t dk = sdesc_sw128(sK, 16, 1024);
-      // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
-      auto issue_s = [&](int j) {
-        const int s = j % C::kNSKT;
-        if (leader) {
-          const uint64_t dks = s == C::kNSK ? sdesc_sw128(sQ, 16, 1024)
-                                            : dk + (uint64_t)((s * C::kKVBytes) >> 4);
+      const uint32_t hi = (uint32_t)(dk >> 32);
+      if (warp == 1) {
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+        const uint32_t k_lo = (uint32_t)dk, q_lo = (uint32_t)sdesc_sw128(sQ, 16, 1024);
+        // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
+        auto issue_s = [&](int j) {
+          const int s = j % C::kNSKT;
+          const uint32_t ks = s == C::kNSK ? q_lo : k_lo + ((uint32_t)(s * C::kKVBytes) >> 4);
           const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ts(dcol, tbase + C::kColQ + kk * 8, dks + off, idS, kk > 0);
+            mma_ts(dcol, tbase + C::kColQ + kk * 8, desc_join(ks + off, hi), idS, kk > 0);
           }
           tc_commit(smem_u32(&bars->k_empty[s]));
           tc_commit(smem_u32(&bars->s_full[j & 1]));
+        };
+        // S_0, S_1, then S_{j+2} as soon as the softmax has read S_j out of
+        // its buffer: S_{j+2} runs on the tensor core while the softmax works on j
+        bool ok = wait(&bars->q_tmem, 0) && wait(&bars->k_full[0], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
         }
-        __syncwarp();
-      };
-      // S_0, S_1, then S_{j+2} as soon as the softmax has read S_j out of
-      // its buffer: S_{j+2} runs on the tensor core while the softmax works on j
-      bool ok = wait2(&bars->q_tmem, 0, &bars->k_full[0], 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 1; ok && j < nb; ++j) {
-        const int ks = j % C::kNSKT;
-        if (j >= 2) {
-          if (!wait2(&bars->s_free[j & 1], ((j - 2) >> 1) & 1, &bars->k_full[ks], (j / C::kNSKT) & 1)) break;
-        } else if (!wait2(&bars->k_full[ks], (j / C::kNSKT) & 1, &bars->k_full[ks], (j / C::kNSKT) & 1)) {
-          break;
+        for (int j = 1; ok && j < nb; ++j) {
+          const int ks = j % C::kNSKT;
+          if (j >= 2 && !wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1)) break;
+          if (!wait(&bars->k_full[ks], (j / C::kNSKT) & 1)) break;
+          tc_fence_after();
+          issue_s(j);
         }
-        tc_fence_after();
-        issue_s(j);
-      }
-    } else {
-      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
-      const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);
-      for (int j = 0; j < nb; ++j) {
-        const int sb = j & 1, vs = j % C::kNSV;
-        if (!wait2(&bars->p_full[sb], (j >> 1) & 1, &bars->v_full[vs], (j / C::kNSV) & 1)) break;
-        tc_fence_after();
-        if (leader) {
-          const uint64_t dvs = dv + (uint64_t)((vs * C::kKVBytes) >> 4);
-          const uint32_t pcol = tbase + C::kColP;
+      } else {
+        constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
+        const uint32_t v_lo = (uint32_t)sdesc_sw128(sV, C::kBoxBytes, 1024);
+        const uint32_t pcol = tbase + C::kColP;
+        for (int j = 0; j < nb; ++j) {
+          const int sb = j & 1, vs = j % C::kNSV;
+          if (!wait(&bars->p_full[sb], (j >> 1) & 1)) break;
+          if (!wait(&bars->v_full[vs], (j / C::kNSV) & 1)) break;
+          tc_fence_after();
+          const uint32_t vb = v_lo + ((uint32_t)(vs * C::kKVBytes) >> 4);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + C::kColO, pcol + kk * 8, dvs + (uint64_t)((kk * 2048) >> 4), idPV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tbase + C::kColO, pcol + kk * 8, desc_join(vb + ((uint32_t)(kk * 2048) >> 4), hi), idPV,
+                   kk > 0 ? 1u : acc0);
           tc_commit(smem_u32(&bars->v_empty[vs]));
           tc_commit(smem_u32(&bars->pv_done[sb]));
         }
-        __syncwarp();
       }
-    }
-    // every MMA issued by this warp has completed before TMEM is freed
-    if (leader) {
+      // every MMA issued by this thread has completed before TMEM is freed
+      uint64_t* done = warp == 1 ? &bars->mma_done : &bars->mma_done_pv;
       int never = 0;
       tc_commit(smem_u32(done));
       mbar_wait_bounded(smem_u32(done), 0, &never, kTimeoutNs);
