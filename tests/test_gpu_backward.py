@@ -78,6 +78,10 @@ EDGE = [
     Workload("bwd-T127-G8", T=127, Hq=16, Hk=2, d=128, L=7),
     Workload("bwd-T200-G1", T=200, Hq=3, Hk=3, d=64, L=33),
     Workload("bwd-T300-G4", T=300, Hq=8, Hk=2, d=128, L=24, seed=5),
+    # many 64-row sub-tiles per key block (both S^T/dP^T buffers reused over many
+    # barrier phases) with a ragged tail, at each head dimension
+    Workload("bwd-T1000-G2-d64", T=1000, Hq=4, Hk=2, d=64, L=8, seed=9),
+    Workload("bwd-T700-G2-d128", T=700, Hq=4, Hk=2, d=128, L=5, seed=11),
 ]
 
 
