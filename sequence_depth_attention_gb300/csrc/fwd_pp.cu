@@ -48,6 +48,7 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kSumBound = 256.0f;         // 2^kRescaleThreshold
 
 constexpr int kTile = 128 * D * 2;  // one 128-row, 64-column box (16 KB)
 constexpr int kOffQ = 0;            // Q_A, Q_B
@@ -362,8 +363,8 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           for (int c = 0; c < BN; ++c) x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;
         }
       }
-      float mx;
-      {
+      // row max of the raw scores (scaled after): three-input max tree
+      auto row_max = [&]() -> float {
         float a1[43];
 #pragma unroll
         for (int i = 0; i < 42; ++i)
@@ -377,8 +378,8 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         float a3[5];
 #pragma unroll
         for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
-        mx = fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
-      }
+        return fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
+      };
       uint32_t pk[BN / 2];
       auto compute_p = [&](float m) -> float {
         const float nbase = (m == -INFINITY) ? 0.f : -m;
@@ -399,15 +400,18 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         f2_split(acc[0], u, w);
         return u + w;
       };
-      // stale-reference fast path, max-first slow path with a lazy rescale of
-      // O and l (as in the d = 128 kernel)
+      // stale-reference fast path checked by the block sum (every p is at
+      // most the sum, so a sum within 2^threshold proves the max did not rise
+      // past it); max-first slow path with a lazy rescale of O and l (as in
+      // the d = 128 kernel)
       float sum = 0.f;
       bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
       if (!slow) {
         sum = compute_p(m_ref);
-        slow = __any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold);
+        slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
       }
       if (slow) {
+        const float mx = row_max();
         const bool need = mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mx : m_ref;

@@ -63,6 +63,7 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kSumBound = 256.0f;         // 2^kRescaleThreshold
 
 template <int D>
 struct Cfg {
@@ -437,19 +438,19 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         return u + w;
       };
       // Fast path: exponentiate against the running reference m_ref right
-      // away and check the block max in the shadow of the exponentials. Only
-      // if some row of the warp has no reference yet, or its max rose by more
-      // than the threshold, fall back to max-first with a rescale of O and l.
-      // The max tree comes first in program order but nothing in the fast
-      // path's exponentials depends on it, so the two interleave.
-      const float mx = row_max();
+      // away. Every p is at most the block's sum, so a sum within 2^threshold
+      // proves no score rose more than the threshold above m_ref, and the
+      // block needs no max at all. Only if some row of the warp has no
+      // reference yet, or its sum exceeds the bound, fall back to max-first
+      // with a rescale of O and l where the max really rose that far.
       float sum = 0.f;
       bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
       if (!slow) {
         sum = compute_p(m_ref);
-        slow = __any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold);
+        slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
       }
       if (slow) {
+        const float mx = row_max();
         const bool need = mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mx : m_ref;
