@@ -206,15 +206,18 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
       };
-      auto issue_sdp = [&](int j) {  // S_j and dP_j; frees V_j when done
-        const int ks = j % C::kNSK, vs = j % C::kNSV;
+      auto issue_s = [&](int j) {  // S_j
+        const int ks = j % C::kNSK;
         const uint32_t kb = k_lo + ((uint32_t)(ks * C::kTileBytes) >> 4);
-        const uint32_t vb = v_lo + ((uint32_t)(vs * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + C::kColS, desc_join(q_lo + off, hi), desc_join(kb + off, hi), idS, kk > 0);
         }
+      };
+      auto issue_dp = [&](int j) {  // dP_j; frees V_j when done, completes block j
+        const int vs = j % C::kNSV;
+        const uint32_t vb = v_lo + ((uint32_t)(vs * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
@@ -235,19 +238,24 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_commit(smem_u32(&bars->k_empty[ks]));
         tc_commit(smem_u32(&bars->dq_done[b]));
       };
-      bool ok = wait(&bars->q_full, 0) && wait(&bars->k_full[0], 0) && wait(&bars->v_full[0], 0);
+      bool ok = wait(&bars->q_full, 0) && wait(&bars->k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_sdp(0);
+        issue_s(0);
+        ok = wait(&bars->v_full[0], 0);
+        if (ok) issue_dp(0);
       }
       for (int j = 0; ok && j < nb; ++j) {
         if (j + 1 < nb) {
-          // S_{j+1}, dP_{j+1} as soon as the softmax holds S_j, dP_j in registers
+          // S_{j+1}, dP_{j+1} as soon as the softmax holds S_j, dP_j in registers;
+          // S needs only K_{j+1}, so it runs while V_{j+1} may still be landing
           if (!wait(&bars->s_free, j & 1)) break;
           if (!wait(&bars->k_full[(j + 1) % C::kNSK], ((j + 1) / C::kNSK) & 1)) break;
+          tc_fence_after();
+          issue_s(j + 1);
           if (!wait(&bars->v_full[(j + 1) % C::kNSV], ((j + 1) / C::kNSV) & 1)) break;
           tc_fence_after();
-          issue_sdp(j + 1);
+          issue_dp(j + 1);
         }
         if (!wait(&bars->ds_full[j & 1], (j >> 1) & 1)) break;
         tc_fence_after();
