@@ -249,8 +249,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (j + 1 < nb) {
           // S_{j+1}, dP_{j+1} as soon as the softmax holds S_j, dP_j in registers;
           // S needs only K_{j+1}, so it runs while V_{j+1} may still be landing
-          if (!wait(&bars->s_free, j & 1)) break;
-          if (!wait(&bars->k_full[(j + 1) % C::kNSK], ((j + 1) / C::kNSK) & 1)) break;
+          uint64_t* kf = &bars->k_full[(j + 1) % C::kNSK];
+          const uint32_t kpar = ((j + 1) / C::kNSK) & 1;
+          if (!mbar_test_both(smem_u32(&bars->s_free), j & 1, smem_u32(kf), kpar)) {
+            if (!wait(&bars->s_free, j & 1)) break;
+            if (!wait(kf, kpar)) break;
+          }
           tc_fence_after();
           issue_s(j + 1);
           if (!wait(&bars->v_full[(j + 1) % C::kNSV], ((j + 1) / C::kNSV) & 1)) break;

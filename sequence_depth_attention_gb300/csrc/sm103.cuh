@@ -60,6 +60,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True if both phases have completed; the two tests are issued together so
+// their latencies overlap, and neither suspends the thread. A false result
+// says nothing about either barrier: wait on each with mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_test_both(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      " and.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(pa), "r"(b), "r"(pb)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after timeout_ns or when *abort becomes non-zero;
 // on timeout it raises *abort. Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
