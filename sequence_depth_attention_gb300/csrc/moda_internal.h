@@ -70,20 +70,17 @@ moda_status report(moda_status s, const char* fmt, ...) __attribute__((format(pr
 // Launchers. Return cudaSuccess or the launch error.
 cudaError_t launch_pack_depth(const void* src, void* dst, int L, int T, int Hk,
                               int d, cudaStream_t stream);
-cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);
 // d = 64: two query tiles per CTA in ping-pong.
 cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream);
 // Depth part on CUDA cores, merged into o and lse that hold the L = 0 result.
 cudaError_t launch_fwd_depth_cc(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
-// The sequence share of dq, added to what the depth kernel wrote (L > 0) or
-// written (L == 0): tcgen05 version (dispatched) and mma.sync version.
+// The sequence share of dq on tcgen05, added to what the depth kernel wrote
+// (L > 0) or written (L == 0).
 cudaError_t launch_bwd_dq_tc(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd_dq_mma(const BwdArgs& a, cudaStream_t stream);
-// dk and dv of the sequence keys: tcgen05 version (dispatched) and mma.sync version.
+// dk and dv of the sequence keys on tcgen05.
 cudaError_t launch_bwd_dkdv_tc(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd_dkdv_mma(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_kv_proj(const KvProjArgs& a, cudaStream_t stream);
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
