@@ -379,22 +379,31 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(smem_u32(&bars->s_free[sb]));
       // mask on raw scores: keep columns [lo, hi) of this block (scale > 0, so
       // masking and the max commute with scaling)
-      {
-        int lo = 0, hi = BN;
-        if (sch.depth) {
-          lo = d_lo - sch.index * BN;
-          hi = d_hi - sch.index * BN;
-        } else {
-          const int k0 = sch.index * BN;
-          if (k0 + BN - 1 > p0) hi = t_mask - k0 + 1;
-        }
-        lo = max(lo, 0);
-        hi = min(hi, BN);
+      if (sch.depth) {
+        // depth block: keep columns [lo, hi), the row's own slots; one validity
+        // word per 32 columns (bit i of word k: column 32k+i), so each column
+        // costs a bit test and a select
+        const int lo = d_lo - sch.index * BN, hi = d_hi - sch.index * BN;
         if (lo > 0 || hi < BN) {
-          const unsigned span = (unsigned)max(hi - lo, 0);
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;  // -inf
+          for (int k = 0; k < BN / 32; ++k) {
+            const int a = min(max(lo - 32 * k, 0), 32), b = min(max(hi - 32 * k, 0), 32);
+            const uint32_t upto_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+            const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+            const uint32_t word = upto_b & ~below_a;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              x[32 * k + i] = (word & (1u << i)) ? x[32 * k + i] : 0xff800000u;  // -inf
+          }
+        }
+      } else {
+        // sequence block: the grouped causal mask keeps columns below hi
+        // (scale > 0, so masking and the max commute with scaling)
+        const int k0 = sch.index * BN;
+        if (k0 + BN - 1 > p0) {
+          const int hi = t_mask - k0 + 1;
+#pragma unroll
+          for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
         }
       }
       // row max of the raw scores (scaled after): three-input max tree, depth 4
