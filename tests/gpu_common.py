@@ -60,10 +60,12 @@ def compare(x, scale, o, lse, ts=None, hs=None):
 
 
 def check_workload(w: Workload, sampled=False, device_inputs=False, q_mul=1.0,
-                   depth_on_cuda_cores=False):
+                   depth_on_cuda_cores=False, prep=None):
     x = make_inputs(w, device="cuda" if device_inputs else "cpu")
     if q_mul != 1.0:
         x["q"] = (x["q"].float() * q_mul).to(torch.bfloat16)
+    if prep is not None:  # reshape the inputs' statistics (same tensors go to the oracle)
+        x = prep(x)
     o, lse = run_cuda(x, w.scale, depth_on_cuda_cores=depth_on_cuda_cores)
     if device_inputs:
         x = {n: t.cpu() for n, t in x.items()}

@@ -90,6 +90,25 @@ def test_peaked_softmax():
     gc.check_workload(Workload("peaked", T=700, Hq=8, Hk=2, d=128, L=12, seed=9), q_mul=4.0)
 
 
+def _key_ramp(x):
+    # key magnitudes grow 0.5x -> 4x along the sequence and q is doubled, so
+    # every row's running max keeps rising: blocks far above the reference
+    # force a rescale of O and l after the first block, and blocks a few log2
+    # units above it push the block sum past its bound without one
+    T = x["k"].shape[0]
+    ramp = torch.linspace(0.5, 4.0, T).view(T, 1, 1)
+    x["k"] = (x["k"].float() * ramp).to(torch.bfloat16)
+    x["q"] = (x["q"].float() * 2.0).to(torch.bfloat16)
+    return x
+
+
+@pytest.mark.parametrize("w", [Workload("ramp-d128", T=1000, Hq=8, Hk=2, d=128, L=12, seed=21),
+                               Workload("ramp-d64", T=700, Hq=8, Hk=2, d=64, L=16, seed=22)],
+                         ids=lambda w: w.name)
+def test_rising_scores_rescale(w):
+    gc.check_workload(w, prep=_key_ramp)
+
+
 def test_depth_slot_permutation_invariance():
     w = Workload("perm", T=300, Hq=8, Hk=2, d=128, L=10, seed=2)
     x = make_inputs(w)
