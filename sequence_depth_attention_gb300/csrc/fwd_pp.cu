@@ -346,21 +346,29 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // S is in registers: the tile's S columns may take its next block
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->s_free[tx]));
-      {
-        int lo = 0, hi = BN;
-        if (sch.depth) {
-          lo = d_lo - sch.index * BN;
-          hi = d_hi - sch.index * BN;
-        } else {
-          const int k0 = sch.index * BN;
-          if (k0 + BN - 1 > p0x) hi = t_mask - k0 + 1;
-        }
-        lo = max(lo, 0);
-        hi = min(hi, BN);
+      if (sch.depth) {
+        // depth block: keep the row's own slots [lo, hi), one validity word per
+        // 32 columns (a bit test and a select per column)
+        const int lo = d_lo - sch.index * BN, hi = d_hi - sch.index * BN;
         if (lo > 0 || hi < BN) {
-          const unsigned span = (unsigned)max(hi - lo, 0);
 #pragma unroll
-          for (int c = 0; c < BN; ++c) x[c] = ((unsigned)(c - lo) < span) ? x[c] : 0xff800000u;
+          for (int k = 0; k < BN / 32; ++k) {
+            const int a = min(max(lo - 32 * k, 0), 32), b = min(max(hi - 32 * k, 0), 32);
+            const uint32_t upto_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+            const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+            const uint32_t word = upto_b & ~below_a;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              x[32 * k + i] = (word & (1u << i)) ? x[32 * k + i] : 0xff800000u;  // -inf
+          }
+        }
+      } else {
+        // sequence block: the grouped causal mask keeps columns below hi
+        const int k0 = sch.index * BN;
+        if (k0 + BN - 1 > p0x) {
+          const int hi = t_mask - k0 + 1;
+#pragma unroll
+          for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
         }
       }
       // row max of the raw scores (scaled after): three-input max tree
