@@ -245,7 +245,10 @@ MODA_API moda_status moda_bwd(const void* q, const void* k, const void* v, const
  *   MODA_ERR_UNSUPPORTED and launch nothing.
  *   The first call on each device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
- *   stream capture.
+ *   stream capture. The address belongs to the device's current context:
+ *   after cudaDeviceReset the next call looks it up again (that call, too,
+ *   should come before any capture). A device that is not an sm_103 part
+ *   gives MODA_ERR_NO_DEVICE before any lookup.
  *   All calls share the one array, which keeps the last call's contents;
  *   each call writes every element it reads, so nothing is cleared between
  *   calls. Calls that overlap on the GPU (other streams, other host threads)

@@ -12,8 +12,10 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its 4 MiB until the process exits. In host code the name
 // g_bwd_scratch is only a host-side stand-in for the symbol, never a device
-// address; its device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.
+// address; its device address is looked up with cudaGetSymbolAddress (with
+// that device current) on the first call on each device, and again whenever
+// the device's current context is not the one it was looked up in (after a
+// cudaDeviceReset the module's variables live in a new context).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,7 +31,11 @@ static __device__ __align__(256) float g_bwd_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  void* ctx = nullptr;
+  float* addr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 
 }  // namespace
 
@@ -43,22 +49,28 @@ extern "C" moda_status moda_bwd_noalloc(const void* q, const void* k, const void
                         "T*Hq = %lld rows exceed the fixed scratch of %lld rows; use moda_bwd "
                         "with a caller workspace",
                         (long long)T * Hq, (long long)kScratchFloats);
+  // the device must be one the library runs on before its symbols are touched
   int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return moda::report(MODA_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  moda_status st = moda::checked_device(&dev);
+  if (st != MODA_OK) return st;
+  if (dev >= kMaxDevices)
+    return moda::report(MODA_ERR_NO_DEVICE, "device ordinal %d; libmoda serves devices 0..%d",
+                        dev, kMaxDevices - 1);
   float* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchEntry& ent = g_scratch[dev];
+    void* ctx = moda::current_context();
+    if (!ent.addr || !ctx || ctx != ent.ctx) {
       void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
       if (e != cudaSuccess || !p)
         return moda::report(MODA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
                             cudaGetErrorString(e));
-      g_scratch_addr[dev] = static_cast<float*>(p);
+      ent.addr = static_cast<float*>(p);
+      ent.ctx = moda::current_context();
     }
-    scratch = g_scratch_addr[dev];
+    scratch = ent.addr;
   }
   // Every element of the scratch that the kernels read is first written by
   // the same call (the delta kernel fills all T*Hq rows), so nothing needs

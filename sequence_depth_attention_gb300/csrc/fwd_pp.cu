@@ -130,8 +130,10 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int G = 1 << p.lgG;
   PairGeom g;
   g.P = BM >> p.lgG;
-  const int pp = p.npairs - 1 - (int)(blockIdx.x / p.Hk);  // longest pair first
-  const int hk = (int)(blockIdx.x % p.Hk);
+  // KV-head-major grid, longest pair first within a head (resident CTAs share
+  // one or two heads' K/V in L2)
+  const int pp = p.npairs - 1 - (int)(blockIdx.x % p.npairs);
+  const int hk = (int)(blockIdx.x / p.npairs);
   g.p0 = pp * 2 * g.P;
   g.npos[0] = min(g.P, p.T - g.p0);
   g.npos[1] = g.p0 + g.P < p.T ? min(g.P, p.T - g.p0 - g.P) : 0;

@@ -24,7 +24,7 @@
 //     unnormalised output O, which lives in TMEM and is accumulated by the
 //     tensor core; o = O / l once at the end, lse = m ln2 + ln l.
 //
-// Roles (8 warps, one CTA per tile, longest tiles first):
+// Roles (8 warps, one CTA per tile; KV-head-major, longest tiles first):
 //   warp 0  lane 0: TMA producer for Q and the K blocks
 //   warp 1  lane 0: tcgen05.mma issuer of S = Q K^T; the whole warp allocates TMEM
 //   warp 2  lane 0: TMA producer for the V blocks
@@ -129,8 +129,11 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = 1 << p.lgG;
   const int P = BM >> p.lgG;  // positions per tile
-  const int tile = p.ntiles - 1 - (int)(blockIdx.x / p.Hk);
-  const int hk = (int)(blockIdx.x % p.Hk);
+  // KV-head-major grid, longest tiles first within a head: the CTAs resident
+  // at one time share one or two heads' K/V, which then stay in L2 while the
+  // tiles stream through them (head-interleaved, they span every head's K/V)
+  const int tile = p.ntiles - 1 - (int)(blockIdx.x % p.ntiles);
+  const int hk = (int)(blockIdx.x / p.ntiles);
   const int p0 = tile * P;
   const int npos = min(P, p.T - p0);
   const int t_last = p0 + npos - 1;

@@ -1,5 +1,6 @@
 // C-ABI entry points of libmoda.so (declared in include/moda.h): argument
 // validation, the per-device kernel error word, and dispatch to the kernels.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,18 +37,30 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
-unsigned int* g_err_ptr[kMaxDevices] = {};
-int g_num_sms[kMaxDevices] = {};
+struct DeviceEntry {
+  void* ctx = nullptr;            // context the cached address belongs to
+  unsigned int* err = nullptr;    // device address of g_moda_err in it
+  int sms = 0;
+};
+DeviceEntry g_dev[kMaxDevices];
 
 // Current device, its error-word address and SM count; checks that it is
-// an sm_103 part (the only target the library is compiled for).
+// an sm_103 part (the only target the library is compiled for). The address
+// is cached per device together with the context it was resolved in, and
+// resolved again when the current context differs (after cudaDeviceReset the
+// runtime creates a new primary context, and the module's variables move).
 moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (e != cudaSuccess || dev < 0)
     return fail(MODA_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= kMaxDevices)
+    return fail(MODA_ERR_NO_DEVICE, "device ordinal %d; libmoda serves devices 0..%d", dev,
+                kMaxDevices - 1);
   std::lock_guard<std::mutex> lk(g_dev_mu);
-  if (!g_err_ptr[dev]) {
+  DeviceEntry& ent = g_dev[dev];
+  void* ctx = moda::current_context();
+  if (!ent.err || !ctx || ctx != ent.ctx) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -59,12 +72,13 @@ moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out) {
     e = cudaGetSymbolAddress(&p, g_moda_err);
     if (e != cudaSuccess || !p)
       return fail(MODA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
-    g_err_ptr[dev] = (unsigned int*)p;
-    g_num_sms[dev] = sms;
+    ent.err = (unsigned int*)p;
+    ent.sms = sms;
+    ent.ctx = moda::current_context();  // bound by now
   }
   *dev_out = dev;
-  *err_out = g_err_ptr[dev];
-  *sms_out = g_num_sms[dev];
+  *err_out = ent.err;
+  *sms_out = ent.sms;
   return MODA_OK;
 }
 
@@ -77,6 +91,27 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace moda {
+void* current_context() {
+  static PFN_cuCtxGetCurrent_v4000 get = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  }();
+  CUcontext c = nullptr;
+  if (!get || get(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+moda_status checked_device(int* dev) {
+  unsigned int* err;
+  int sms;
+  return device_state(dev, &err, &sms);
+}
+
 moda_status report(moda_status s, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

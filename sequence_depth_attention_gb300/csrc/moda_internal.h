@@ -63,6 +63,15 @@ struct KvProjArgs {
 // Kernel error codes latched into the device error word (first one wins).
 enum : unsigned int { kErrNone = 0, kErrTimeout = MODA_ERR_TIMEOUT };
 
+// The calling thread's current CUDA context (nullptr if none is bound):
+// device addresses of module variables are valid only in the context they
+// were looked up in.
+void* current_context();
+
+// The current device after checking that it is an sm_103 part; otherwise
+// MODA_ERR_NO_DEVICE (or MODA_ERR_CUDA) with the detail set.
+moda_status checked_device(int* dev);
+
 // Sets the calling thread's last-error detail (see moda_last_error_detail)
 // and returns s.
 moda_status report(moda_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));

@@ -1,5 +1,5 @@
-// Warp-level MMA helpers (mma.sync m16n8k16 bf16 -> fp32, ldmatrix, cp.async)
-// shared by the warp-MMA kernels.
+// Warp-level MMA helpers (mma.sync m16n8k16 bf16 -> fp32, ldmatrix) used by
+// the decode kernel, whose per-token work is too small for tcgen05 tiles.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -7,25 +7,6 @@
 
 namespace moda {
 namespace wmma16 {
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// element offset of (row, col) in a [rows][D] bf16 tile whose 16-byte chunks
-// are XOR-swizzled by (row & 7) so ldmatrix rows hit distinct banks
-template <int D>
-__device__ __forceinline__ int swz(int row, int col) {
-  return row * D + ((((col >> 3) ^ (row & 7))) << 3) + (col & 7);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 -> zero-fill, nothing read
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"

@@ -1,7 +1,11 @@
 """moda_bwd_noalloc -- the backward for callers that cannot give the library
 device memory for scratch -- must agree with moda_bwd (caller workspace) on
-the same inputs, on two calls in a row (the second reuses the scratch the
-first left behind). Collected last so that a failure here does not hide the
+the same inputs, on two calls in a row. Before the checked calls, one call
+with a different upstream gradient fills the shared scratch with other
+values, so a row the delta kernel failed to write would show up as wrong
+gradients. Both entry points run the same deterministic kernels (no atomics),
+so the gradients must agree bit for bit, and a fortiori within the backward
+tests' tolerance. Collected last so that a failure here does not hide the
 other tests in a run that stops at the first failure."""
 import numpy as np
 import pytest
@@ -41,8 +45,12 @@ def test_noalloc_backward_matches_workspace_backward(w):
     o, lse = moda.moda_fwd(x["q"], x["k"], x["v"], kd, vd, w.scale)
     g = torch.Generator(device="cuda").manual_seed(5)
     dO = torch.randn((w.T, w.Hq, w.d), generator=g, device="cuda").to(torch.bfloat16)
+    dO_other = torch.randn((w.T, w.Hq, w.d), generator=g, device="cuda").to(torch.bfloat16)
     args = (x["q"], x["k"], x["v"], kd, vd, o, lse, dO, w.scale)
     ref = moda.moda_bwd(*args)
+    # leaves the scratch holding the deltas of another dO
+    moda.moda_bwd_noalloc(x["q"], x["k"], x["v"], kd, vd, o, lse, dO_other, w.scale,
+                          grads=_grads(w))
     for _ in range(2):
         got = moda.moda_bwd_noalloc(*args, grads=_grads(w))
         torch.cuda.synchronize()
@@ -53,6 +61,7 @@ def test_noalloc_backward_matches_workspace_backward(w):
             r, a = r.cpu().numpy(), a.cpu().numpy()
             assert np.isfinite(a).all()
             assert np.max(np.abs(a - r)) <= REL * max(np.max(np.abs(r)), 1e-30)
+            assert np.array_equal(a, r)
 
 
 def test_noalloc_rejects_oversize():
