@@ -111,6 +111,57 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// p = 2^(s*sl - m) for the N raw scores x (fp32 bits) as bf16 pairs into pk;
+// returns the fp32 sum. One packed FMA per pair, then the exponential unit;
+// the sum through eight packed accumulators.
+template <int N>
+__device__ __forceinline__ float exp_block(const uint32_t* x, uint32_t* pk, float sl, float m) {
+  static_assert(N >= 16 && N % 16 == 0, "whole accumulator rounds");
+  const float nbase = (m == -INFINITY) ? 0.f : -m;
+  const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
+  uint64_t acc[8];
+#pragma unroll
+  for (int c = 0; c < N / 2; ++c) {
+    float u, w;
+    f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2), u, w);
+    const float e0 = ex2_approx(u), e1 = ex2_approx(w);
+    pk[c] = pack_bf16x2(e0, e1);
+    acc[c & 7] = c < 8 ? f2(e0, e1) : fadd2(acc[c & 7], f2(e0, e1));
+  }
+  acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  acc[4] = fadd2(fadd2(acc[4], acc[5]), fadd2(acc[6], acc[7]));
+  acc[0] = fadd2(acc[0], acc[4]);
+  float u, w;
+  f2_split(acc[0], u, w);
+  return u + w;
+}
+
+// Row maximum of raw scores by three-input max trees.
+__device__ __forceinline__ float raw_max128(const uint32_t* x) {
+  float a1[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i)
+    a1[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]), __uint_as_float(x[3 * i + 2]));
+  a1[42] = fmaxf(__uint_as_float(x[126]), __uint_as_float(x[127]));
+  float a2[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) a2[i] = max3f(a1[3 * i], a1[3 * i + 1], a1[3 * i + 2]);
+  a2[14] = a1[42];
+  float a3[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
+  return fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4]));
+}
+__device__ __forceinline__ float raw_max32(const uint32_t* x) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i)
+    a[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]), __uint_as_float(x[3 * i + 2]));
+  a[10] = fmaxf(__uint_as_float(x[30]), __uint_as_float(x[31]));
+  return fmaxf(max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), max3f(a[6], a[7], a[8])),
+               fmaxf(a[9], a[10]));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -137,8 +188,15 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int p0 = tile * P;
   const int npos = min(P, p.T - p0);
   const int t_last = p0 + npos - 1;
-  const int nd = npos * p.L;
-  const int n_depth = (nd + BN - 1) / BN;
+  // Depth blocks, one 32-row word per softmax warp: warp w (rows 32w..32w+31,
+  // positions p0 + w*PW .. + PW) owns columns [32w, 32w+32) of every depth
+  // block, filled with the next 32 of its own RW = PW*L packed depth rows.
+  // Each row's slots then fall in its own warp's word, so a softmax warp
+  // exponentiates 32 columns of a depth block instead of 128; the tensor core
+  // still computes the whole block (the other words of a row are masked).
+  const int PW = P >> 2;                 // positions per softmax warp
+  const int RW = PW * p.L;               // packed depth rows per warp
+  const int n_depth = (min(npos, PW) * p.L + 31) / 32;
   const int nb = n_depth + t_last / BN + 1;
   const int depth_row0 = (hk * p.T + p0) * p.L;  // first packed depth row of the tile
   // Block schedule: the n_depth depth blocks are spread evenly among the
@@ -236,9 +294,13 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_arrive_expect_tx(fb, C::kKVBytes);
         const uint32_t dst = (is_k && s == C::kNSK) ? sQ : sbase + s * C::kKVBytes;
         if (sch.depth) {
-          for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_2d_hint(dst + c * C::kBoxBytes, dep_map, fb, c * 64, depth_row0 + sch.index * BN,
-                             pol_once);
+          // four 32-row words: rows [32w, 32w+32) of the stage hold warp w's
+          // packed depth rows 32*index .. +32 (128-byte swizzle atoms are 8
+          // rows, so a word starts on an atom boundary)
+          for (int w = 0; w < 4; ++w)
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_2d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64,
+                               depth_row0 + w * RW + sch.index * 32, pol_once);
         } else {
           for (int c = 0; c < C::kBoxes; ++c)
             tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, sch.index * BN);
@@ -336,8 +398,9 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int h_row = hk * G + (row & (G - 1));
     const bool valid = t_row < p.T;
     const int t_mask = min(t_row, p.T - 1);
-    const int d_lo = lp * p.L;
-    const int d_hi = min(d_lo + p.L, nd);
+    const int wq = warp & 3;                    // this warp's word of a depth block
+    const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's RW rows
+    const int dw_n = valid ? p.L : 0;            // rows past T keep no depth column
     const float sl = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -362,6 +425,42 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(smem_u32(&bars->q_tmem));
     }
+    // Rescale O and l to a new reference when a block's raw max mx (log2
+    // units) rose more than the threshold above it; false on a timeout.
+    auto rescale = [&](float mx, int j) -> bool {
+      const bool need = mx > m_ref + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_ref;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+        if (j > 0) {
+          // O holds blocks 0..j-1: wait for the last of them, then rescale it
+          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
+            tmem_ld32(ta, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(ta, r);
+          }
+          tmem_st_wait();
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      return true;
+    };
+    // Fast path of every block: exponentiate against the running reference
+    // m_ref right away. Every p is at most the block's sum, so a sum within
+    // 2^threshold proves no score rose more than the threshold above m_ref,
+    // and the block needs no max at all. Only if some row of the warp has no
+    // reference yet, or its sum exceeds the bound, fall back to max-first with
+    // a rescale of O and l where the max really rose that far.
+    const uint32_t zeros[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    bool p_zero = false;  // this warp's P columns outside its depth word hold zeros
     Sched sch;
     for (int j = 0; ok && j < nb; ++j) {
       sch.next(n_depth, nb);
@@ -371,140 +470,96 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         break;
       }
       tc_fence_after();
-      // S row of this thread: 128 raw fp32 scores held as bits in registers
-      uint32_t x[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
-      tmem_ld_wait();
-      // S_j is in registers: its TMEM buffer may take S_{j+2}
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free[sb]));
-      // mask on raw scores: keep columns [lo, hi) of this block (scale > 0, so
-      // masking and the max commute with scaling)
+      const uint32_t pcol = tmem_addr(tbase, lane_base, C::kColP);
+      float sum = 0.f;
       if (sch.depth) {
-        // depth block: keep columns [lo, hi), the row's own slots; one validity
-        // word per 32 columns (bit i of word k: column 32k+i), so each column
-        // costs a bit test and a select
-        const int lo = d_lo - sch.index * BN, hi = d_hi - sch.index * BN;
-        if (lo > 0 || hi < BN) {
+        // depth block: only this warp's word of 32 columns can hold its rows'
+        // slots; mask (on raw scores, scale > 0) to the row's own slots with
+        // one validity word, a bit test and a select per column
+        uint32_t xs[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + wq * 32), xs);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+        const int lo = dw_lo - sch.index * 32, hi = lo + dw_n;
+        const int a = min(max(lo, 0), 32), b = min(max(hi, 0), 32);
+        const uint32_t word = (b >= 32 ? 0xffffffffu : (1u << b) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
 #pragma unroll
-          for (int k = 0; k < BN / 32; ++k) {
-            const int a = min(max(lo - 32 * k, 0), 32), b = min(max(hi - 32 * k, 0), 32);
-            const uint32_t upto_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
-            const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
-            const uint32_t word = upto_b & ~below_a;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              x[32 * k + i] = (word & (1u << i)) ? x[32 * k + i] : 0xff800000u;  // -inf
-          }
+        for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
+        uint32_t pk[16];
+        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          sum = exp_block<32>(xs, pk, sl, m_ref);
+          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
         }
+        if (slow) {
+          if (!rescale(raw_max32(xs) * sl, j)) {
+            ok = false;
+            break;
+          }
+          sum = exp_block<32>(xs, pk, sl, m_ref);
+        }
+        l += sum;
+        // P_j overwrites P_{j-1}: the tensor core must have consumed it
+        if (j >= 1) {
+          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(pcol + wq * 16, pk);
+        if (!p_zero) {
+          for (int k = 0; k < 4; ++k)
+            if (k != wq) tmem_st16(pcol + k * 16, zeros);
+        }
+        p_zero = true;
       } else {
-        // sequence block: the grouped causal mask keeps columns below hi
-        // (scale > 0, so masking and the max commute with scaling)
+        // sequence block: S row of this thread, 128 raw fp32 scores as bits
+        uint32_t x[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
+        tmem_ld_wait();
+        // S_j is in registers: its TMEM buffer may take S_{j+2}
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+        // the grouped causal mask keeps columns below hi (on raw scores:
+        // scale > 0, so masking and the max commute with scaling)
         const int k0 = sch.index * BN;
         if (k0 + BN - 1 > p0) {
           const int hi = t_mask - k0 + 1;
 #pragma unroll
           for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
         }
-      }
-      // row max of the raw scores (scaled after): three-input max tree, depth 4
-      auto row_max = [&]() -> float {
-        float a1[43];
-#pragma unroll
-        for (int i = 0; i < 42; ++i)
-          a1[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]),
-                        __uint_as_float(x[3 * i + 2]));
-        a1[42] = fmaxf(__uint_as_float(x[126]), __uint_as_float(x[127]));
-        float a2[15];
-#pragma unroll
-        for (int i = 0; i < 14; ++i) a2[i] = max3f(a1[3 * i], a1[3 * i + 1], a1[3 * i + 2]);
-        a2[14] = a1[42];
-        float a3[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
-        return fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
-      };
-      // p = 2^(s*sl - m) as bf16 pairs into pk; returns the fp32 row sum.
-      // One packed FMA per pair, then the exponential unit; packed-add tree.
-      uint32_t pk[BN / 2];
-      auto compute_p = [&](float m) -> float {
-        const float nbase = (m == -INFINITY) ? 0.f : -m;
-        const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
-        uint64_t acc[8];
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          float u, w;
-          f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2),
-                   u, w);
-          const float e0 = ex2_approx(u), e1 = ex2_approx(w);
-          pk[c] = pack_bf16x2(e0, e1);
-          acc[c & 7] = c < 8 ? f2(e0, e1) : fadd2(acc[c & 7], f2(e0, e1));
+        uint32_t pk[BN / 2];
+        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          sum = exp_block<BN>(x, pk, sl, m_ref);
+          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
         }
-        acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-        acc[4] = fadd2(fadd2(acc[4], acc[5]), fadd2(acc[6], acc[7]));
-        acc[0] = fadd2(acc[0], acc[4]);
-        float u, w;
-        f2_split(acc[0], u, w);
-        return u + w;
-      };
-      // Fast path: exponentiate against the running reference m_ref right
-      // away. Every p is at most the block's sum, so a sum within 2^threshold
-      // proves no score rose more than the threshold above m_ref, and the
-      // block needs no max at all. Only if some row of the warp has no
-      // reference yet, or its sum exceeds the bound, fall back to max-first
-      // with a rescale of O and l where the max really rose that far.
-      float sum = 0.f;
-      bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
-      if (!slow) {
-        sum = compute_p(m_ref);
-        slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
-      }
-      if (slow) {
-        const float mx = row_max();
-        const bool need = mx > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mx : m_ref;
-          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-          if (j > 0) {
-            // O holds blocks 0..j-1: wait for the last of them, then rescale it
-            if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
-              tmem_ld32(ta, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(ta, r);
-            }
-            tmem_st_wait();
+        if (slow) {
+          if (!rescale(raw_max128(x) * sl, j)) {
+            ok = false;
+            break;
           }
-          l *= alpha;
-          m_ref = m_new;
+          sum = exp_block<BN>(x, pk, sl, m_ref);
         }
-        sum = compute_p(m_ref);
-      }
-      l += sum;
-      // P_j overwrites P_{j-1}: the tensor core must have consumed it (the
-      // slow path above may have waited for it already; the phase test is
-      // idempotent)
-      if (j >= 1) {
-        if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
-          ok = false;
-          break;
+        l += sum;
+        // P_j overwrites P_{j-1}: the tensor core must have consumed it (the
+        // slow path above may have waited for it already; the phase test is
+        // idempotent)
+        if (j >= 1) {
+          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-      }
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c)
-        tmem_st32(tmem_addr(tbase, lane_base, C::kColP + c * 32), pk + c * 32);
+        for (int c = 0; c < BN / 64; ++c) tmem_st32(pcol + c * 32, pk + c * 32);
+        p_zero = false;
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[sb]));
@@ -570,7 +625,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   if (a.L > 0) {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
     const uint64_t str[1] = {row};
-    const uint32_t box[2] = {64, BN};
+    const uint32_t box[2] = {64, 32};  // one softmax warp's word of a depth block
     if (encode_bf16_sw128(&tkd, a.kd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_bf16_sw128(&tvd, a.vd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   } else {

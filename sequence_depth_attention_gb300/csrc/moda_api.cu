@@ -263,8 +263,10 @@ static moda_status prepare_fwd(const void* q, const void* k, const void* v, cons
     return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
   if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
   if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
-  if ((int64_t)Hk * T * L > 0x7fffffffLL)
-    return fail(MODA_ERR_UNSUPPORTED, "Hk*T*L = %lld packed depth rows exceed 2^31 - 1",
+  // the kernels address packed depth rows with 32-bit coordinates, and a
+  // tile's depth blocks may reach up to 128*L rows past its last own row
+  if ((int64_t)Hk * T * L + 128LL * L > 0x7fffffffLL)
+    return fail(MODA_ERR_UNSUPPORTED, "Hk*T*L = %lld packed depth rows exceed 2^31 - 1 - 128*L",
                 (long long)Hk * T * L);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (L > 0 && (!aligned16(kd) || !aligned16(vd))) || (lse && !aligned16(lse)))
