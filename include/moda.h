@@ -95,6 +95,81 @@ MODA_API moda_status moda_depth_write(const void* src, void* dst, int T, int Hk,
                                       int slot, moda_stream_t stream);
 
 /*
+ * Bounded depth KV cache (summary, Sec. 6.2 "bounded depth KV slot cache"):
+ * the packed streams hold a fixed budget of S slots (S much smaller than the
+ * number of depth entries a deep model writes), and a policy decides which
+ * entries stay. The pages name three policies without defining them further:
+ * keep the top S entries by utility, keep a sliding window of the most recent
+ * entries, or a hybrid that reserves part of the slots for recent entries and
+ * gives the rest to high-scoring ones. Readings taken here:
+ *   - an entry is one layer's depth K/V (one slot index for all heads and
+ *     positions); its age is its write order;
+ *   - its utility is the depth probability mass it received in the latest
+ *     read of the cache (moda_depth_mass, summed over KV heads); a new entry
+ *     has not been read, so it is always admitted and a cached one leaves;
+ *   - `recent` = R slots are reserved for the R most recent entries, the new
+ *     one included (R >= S: sliding window; R <= 1: top-S by utility); of
+ *     the other entries the one with the least utility leaves (equal
+ *     utilities: the older, then the lower slot).
+ * A layer loop runs entirely on the stream, with no host round trip:
+ *   moda_fwd(q, k, v, kd, vd, ..., L = slots filled, o, lse)
+ *   moda_depth_mass(q, kd, lse, ..., mass)         (when all S are filled)
+ *   moda_depth_cache_admit(slot_age, mass, Hk, S, R, layer, slot)
+ *   moda_depth_write_at(k_layer, kd, ..., slot); moda_depth_write_at(v_layer, vd, ..., slot)
+ * Slots fill in order 0, 1, ... while any is empty, so the first L filled
+ * slots are always slots 0..L-1.
+ */
+
+/*
+ * moda_depth_mass -- how much the queries of one layer read each depth slot:
+ *   mass[hk][l] = sum over t < T and the G heads h of group hk of
+ *                 exp(scale * q[t,h,:].kd[hk,t,l,:] - lse[t,h])
+ * i.e. the probability the joint softmax of moda_fwd gives slot l, summed
+ * over the rows of KV head hk.
+ *   q, kd, scale  as passed to moda_fwd (kd packed [Hk, T, L, d])
+ *   lse           [T, Hq] fp32, the lse moda_fwd returned for them
+ *   mass          [Hk, L] fp32 output
+ *   workspace     caller-owned device scratch of at least
+ *                 moda_depth_mass_workspace_bytes(T, Hk, L) bytes
+ * Deterministic: per-block partial sums are added in a fixed order.
+ * Supported: as moda_fwd, with 1 <= L. Errors: INVALID_ARG, UNSUPPORTED,
+ * MISALIGNED, CUDA.
+ */
+MODA_API size_t moda_depth_mass_workspace_bytes(int T, int Hk, int L);
+MODA_API moda_status moda_depth_mass(const void* q, const void* kd, const float* lse, int T,
+                                     int Hq, int Hk, int d, int L, float scale, float* mass,
+                                     float* workspace, size_t workspace_bytes,
+                                     moda_stream_t stream);
+
+/*
+ * moda_depth_cache_admit -- chooses the slot that the entry of age `new_age`
+ * goes into, by the policy above, and records it: slot_age[*slot] = new_age.
+ *   slot_age  [S] int32 device memory, the age of the entry in each slot, -1
+ *             for an empty slot (initialise to -1); updated in place
+ *   mass      [Hk, S] fp32 device memory from moda_depth_mass over the S
+ *             slots; read only when no slot is empty. Utility of slot s:
+ *             the fp32 sum of mass[0][s], mass[1][s], ... in head order;
+ *             NaN orders as the largest
+ *   recent    R >= 0; new_age >= 0, larger than every age in the cache
+ *   slot      one int32 of device memory, receives the chosen slot
+ * One small kernel; the result is ready when the stream is. S <= 1024.
+ * Errors: INVALID_ARG, UNSUPPORTED (S), MISALIGNED, CUDA.
+ */
+MODA_API moda_status moda_depth_cache_admit(int* slot_age, const float* mass, int Hk, int S,
+                                            int recent, int new_age, int* slot,
+                                            moda_stream_t stream);
+
+/*
+ * moda_depth_write_at -- moda_depth_write with the slot index read from
+ * device memory when the kernel runs (as moda_depth_cache_admit leaves it),
+ * so the write needs no host round trip. A slot outside [0, L) writes
+ * nothing and latches MODA_ERR_INVALID_ARG in the device error word
+ * (moda_get_device_error). Other arguments and errors as moda_depth_write.
+ */
+MODA_API moda_status moda_depth_write_at(const void* src, void* dst, int T, int Hk, int d,
+                                         int L, const int* slot, moda_stream_t stream);
+
+/*
  * moda_kv_proj_write -- an FFN layer's depth keys and values, projected from
  * the FFN's input and written straight into slot `slot` of the packed depth
  * streams (reading notes Sec. 二.3: the FFN branch adds a KV projection of its

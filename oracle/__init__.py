@@ -23,9 +23,15 @@ q[T,Hq,d], k/v[T,Hk,d] and the UNPACKED depth stream kd/vd[L,T,Hk,d].
 FFN's input (reading notes Sec. 二.3; summary Sec. 2.2, the "write" step):
 out[t, n] = sum_c x[t, c] * w[n, c] in fp64.
 
+``Oracle.depth_mass`` is the utility of the bounded depth cache (summary
+Sec. 6.2): the probability mass the joint softmax gives each depth slot,
+summed over the rows of each KV head; ``oracle.depth_cache`` is the cache's
+slot choice in plain Python.
+
 Pins (what ties this oracle to the pages and the mathematics rather than to
-itself) are in ``tests/test_oracle_pins.py``, ``tests/test_oracle_bwd.py`` and
-``tests/test_oracle_kvproj.py``; every function here is pinned.
+itself) are in ``tests/test_oracle_pins.py``, ``tests/test_oracle_bwd.py``,
+``tests/test_oracle_kvproj.py`` and ``tests/test_oracle_cache.py``; every
+function here is pinned.
 """
 from __future__ import annotations
 
@@ -108,6 +114,9 @@ class Oracle:
         lib.moda_oracle_bwd_rows.restype = ctypes.c_int
         lib.moda_oracle_kv_proj.argtypes = [u16p, u16p, i, i, i, i64p, ctypes.c_int64, f64p]
         lib.moda_oracle_kv_proj.restype = ctypes.c_int
+        lib.moda_oracle_depth_mass.argtypes = [u16p] * 5 + [i] * 5 + [
+            ctypes.c_double, i64p, i64p, ctypes.c_int64, f64p, i]
+        lib.moda_oracle_depth_mass.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -207,6 +216,28 @@ class Oracle:
         return dq, dk, dv, dkd, dvd
 
 
+    def depth_mass(self, q, k, v, kd, vd, scale, ts=None, hs=None, nthreads: int = 1):
+        """Depth probability mass [Hk, L] float64: entry (hk, l) sums p(slot l)
+        over the rows (ts[i], hs[i]) of KV head hk (every row when ts is None)."""
+        arrs, (T, Hq, Hk, d, L) = self._prep(q, k, v, kd, vd)
+        if L < 1:
+            raise ValueError("depth_mass needs L >= 1")
+        if ts is None:
+            tt, hh = np.meshgrid(np.arange(T), np.arange(Hq), indexing="ij")
+            ts, hs = tt.reshape(-1), hh.reshape(-1)
+        ts = np.ascontiguousarray(ts, dtype=np.int64).reshape(-1)
+        hs = np.ascontiguousarray(hs, dtype=np.int64).reshape(-1)
+        if ts.shape != hs.shape:
+            raise ValueError("ts and hs must have the same length")
+        mass = np.zeros((Hk, L), np.float64)
+        rc = self._lib.moda_oracle_depth_mass(
+            *(_ptr(a, ctypes.c_uint16) for a in arrs), T, Hq, Hk, d, L, float(scale),
+            _ptr(ts, ctypes.c_int64), _ptr(hs, ctypes.c_int64), ts.shape[0],
+            _ptr(mass, ctypes.c_double), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"moda_oracle_depth_mass failed with {rc}")
+        return mass
+
     def kv_proj(self, x, w, rows=None):
         """Linear depth-KV projection of an FFN layer's input: x [T,Dm] and
         w [N,Dm] (bf16 bits, one weight row per output feature). Returns
@@ -254,3 +285,7 @@ def backward(*args, **kw):
 
 def kv_proj(*args, **kw):
     return default().kv_proj(*args, **kw)
+
+
+def depth_mass(*args, **kw):
+    return default().depth_mass(*args, **kw)

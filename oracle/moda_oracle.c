@@ -490,3 +490,100 @@ int moda_oracle_kv_proj(const uint16_t* x, const uint16_t* w, int T, int Dm, int
   }
   return 0;
 }
+
+/*
+ * Depth probability mass: how much the queries of one layer read each depth
+ * slot.
+ *
+ * The bounded depth cache (summary, Sec. 6.2 "bounded depth KV slot cache")
+ * keeps a fixed budget of S slots and, in its dynamic-selection form, scores
+ * the cached entries by utility and keeps the top S. The pages give no
+ * formula for the utility. Reading: the probability mass that the joint
+ * softmax of Sec. 2.2 gives the slot, summed over the rows that read it,
+ *   mass[hk*L + l] = sum over listed rows (t, h) with floor(h/G) = hk of
+ *                    p_{t,h}(depth slot l),
+ * p_{t,h} being the joint row of moda_oracle_row (its entry t + 1 + l).
+ * Rows are (ts[i], hs[i]) for i < n; threads accumulate privately and the
+ * copies are summed in thread order. Returns 0, -1 on a bad argument, -2 on
+ * allocation failure.
+ */
+typedef struct {
+  const uint16_t *q, *k, *v, *kd, *vd;
+  int T, Hq, Hk, d, L;
+  double scale;
+  const int64_t *ts, *hs;
+  int64_t begin, end;
+  double* mass; /* private [Hk*L] */
+  int status;
+} mass_job;
+
+static void* mass_worker(void* arg) {
+  mass_job* jb = (mass_job*)arg;
+  jb->status = 0;
+  const int G = jb->Hq / jb->Hk;
+  double* o = (double*)malloc((size_t)jb->d * sizeof(double));
+  double* p = (double*)malloc(((size_t)jb->T + (size_t)jb->L) * sizeof(double));
+  if (!o || !p) {
+    jb->status = -2;
+    free(o);
+    free(p);
+    return NULL;
+  }
+  for (int64_t i = jb->begin; i < jb->end; ++i) {
+    const int t = (int)jb->ts[i], h = (int)jb->hs[i];
+    double lse;
+    int rc = moda_oracle_row(jb->q, jb->k, jb->v, jb->kd, jb->vd, jb->T, jb->Hq, jb->Hk, jb->d,
+                             jb->L, jb->scale, t, h, o, &lse, p);
+    if (rc != 0) {
+      jb->status = rc;
+      break;
+    }
+    double* m = jb->mass + (int64_t)(h / G) * jb->L;
+    for (int l = 0; l < jb->L; ++l) m[l] += p[t + 1 + l];
+  }
+  free(o);
+  free(p);
+  return NULL;
+}
+
+int moda_oracle_depth_mass(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint16_t* kd, const uint16_t* vd, int T, int Hq, int Hk, int d,
+                           int L, double scale, const int64_t* ts, const int64_t* hs, int64_t n,
+                           double* mass, int nthreads) {
+  if (n < 0 || L < 1 || Hk < 1 || Hq % Hk != 0 || !mass) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 1024) nthreads = 1024;
+  if ((int64_t)nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+  const size_t nm = (size_t)Hk * L;
+  mass_job* jobs = (mass_job*)calloc((size_t)nthreads, sizeof(mass_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  double* priv = (double*)calloc((size_t)nthreads * nm, sizeof(double));
+  if (!jobs || !th || !priv) {
+    free(jobs); free(th); free(priv);
+    return -2;
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    mass_job* jb = &jobs[i];
+    jb->q = q; jb->k = k; jb->v = v; jb->kd = kd; jb->vd = vd;
+    jb->T = T; jb->Hq = Hq; jb->Hk = Hk; jb->d = d; jb->L = L; jb->scale = scale;
+    jb->ts = ts; jb->hs = hs;
+    jb->begin = n * i / nthreads;
+    jb->end = n * (i + 1) / nthreads;
+    jb->mass = priv + (size_t)i * nm;
+  }
+  int started = 0;
+  if (nthreads > 1)
+    for (int i = 0; i < nthreads; ++i) {
+      if (pthread_create(&th[i], NULL, mass_worker, &jobs[i]) != 0) break;
+      ++started;
+    }
+  for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+  for (int i = started; i < nthreads; ++i) mass_worker(&jobs[i]);
+  int status = 0;
+  for (int i = 0; i < nthreads && status == 0; ++i) status = jobs[i].status;
+  memset(mass, 0, nm * sizeof(double));
+  for (int i = 0; i < nthreads; ++i)
+    for (size_t e = 0; e < nm; ++e) mass[e] += jobs[i].mass[e];
+  free(jobs); free(th); free(priv);
+  return status;
+}

@@ -24,8 +24,9 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
            6: "MODA_ERR_NO_DEVICE"}
 
 # every symbol include/moda.h declares
-EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_kv_proj_write", "moda_fwd",
-           "moda_fwd_depth_cc", "moda_decode",
+EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_depth_write_at", "moda_depth_mass",
+           "moda_depth_mass_workspace_bytes", "moda_depth_cache_admit", "moda_kv_proj_write",
+           "moda_fwd", "moda_fwd_depth_cc", "moda_decode",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
@@ -61,6 +62,14 @@ def load():
         lib.moda_kv_proj_write.restype = i
         lib.moda_kv_proj_write.argtypes = [vp, vp, vp] + [i] * 6 + [vp, vp, vp]
         lib.moda_depth_write.restype = i
+        lib.moda_depth_write_at.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        lib.moda_depth_write_at.restype = i
+        lib.moda_depth_mass_workspace_bytes.argtypes = [i, i, i]
+        lib.moda_depth_mass_workspace_bytes.restype = ctypes.c_size_t
+        lib.moda_depth_mass.argtypes = [vp, vp, vp] + [i] * 5 + [f, vp, vp, ctypes.c_size_t, vp]
+        lib.moda_depth_mass.restype = i
+        lib.moda_depth_cache_admit.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        lib.moda_depth_cache_admit.restype = i
         lib.moda_decode_workspace_bytes.argtypes = [i, i, i]
         lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.moda_decode.argtypes = [vp] * 5 + [ctypes.c_longlong] + [i] * 5 + [f, vp, vp, vp,
@@ -153,6 +162,66 @@ def moda_depth_write(src: torch.Tensor, dst: torch.Tensor, slot: int, stream=Non
     st = load().moda_depth_write(_ptr(src), _ptr(dst), T, Hk, d, L, int(slot), _stream(stream))
     _check(st, "moda_depth_write")
     return dst
+
+
+def moda_depth_write_at(src: torch.Tensor, dst: torch.Tensor, slot: torch.Tensor, stream=None):
+    """dst[:, :, slot[0], :] = src permuted, with the slot index read from the
+    int32 device tensor `slot` when the kernel runs."""
+    _need(src, "src"), _need(dst, "dst")
+    _need(slot, "slot", torch.int32)
+    Hk, T, L, d = dst.shape
+    if tuple(src.shape) != (T, Hk, d):
+        raise ValueError(f"src must be [T,Hk,d] = {(T, Hk, d)}")
+    st = load().moda_depth_write_at(_ptr(src), _ptr(dst), T, Hk, d, L, _ptr(slot),
+                                    _stream(stream))
+    _check(st, "moda_depth_write_at")
+    return dst
+
+
+def moda_depth_mass_workspace_bytes(T: int, Hk: int, L: int) -> int:
+    return int(load().moda_depth_mass_workspace_bytes(int(T), int(Hk), int(L)))
+
+
+def moda_depth_mass(q, kd, lse, scale: float, mass=None, workspace=None, stream=None):
+    """Probability mass [Hk, L] (fp32) that the joint softmax of moda_fwd gives
+    each depth slot, summed over the rows of each KV head; lse is the one
+    moda_fwd returned for q and kd (packed [Hk,T,L,d])."""
+    _need(q, "q"), _need(kd, "kd")
+    _need(lse, "lse", torch.float32)
+    T, Hq, d = q.shape
+    Hk, _, L, _ = kd.shape
+    if mass is None:
+        mass = torch.empty((Hk, L), dtype=torch.float32, device=q.device)
+    _need(mass, "mass", torch.float32)
+    nbytes = moda_depth_mass_workspace_bytes(T, Hk, L)
+    if workspace is None:
+        workspace = torch.empty(((nbytes + 3) // 4,), dtype=torch.float32, device=q.device)
+    _need(workspace, "workspace", torch.float32)
+    st = load().moda_depth_mass(_ptr(q), _ptr(kd), _ptr(lse), T, Hq, Hk, d, L, float(scale),
+                                _ptr(mass), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "moda_depth_mass")
+    return mass
+
+
+def moda_depth_cache_admit(slot_age: torch.Tensor, mass: torch.Tensor, recent: int, new_age: int,
+                           slot=None, stream=None):
+    """Chooses the slot for the entry of age new_age (bounded depth cache) and
+    records it in slot_age (int32 [S], -1 = empty); mass is [Hk, S] fp32.
+    Returns the int32 device tensor holding the slot."""
+    _need(slot_age, "slot_age", torch.int32)
+    _need(mass, "mass", torch.float32)
+    S = slot_age.shape[0]
+    Hk = mass.shape[0]
+    if tuple(mass.shape) != (Hk, S):
+        raise ValueError(f"mass must be [Hk, S] with S = {S}")
+    if slot is None:
+        slot = torch.empty((1,), dtype=torch.int32, device=slot_age.device)
+    _need(slot, "slot", torch.int32)
+    st = load().moda_depth_cache_admit(_ptr(slot_age), _ptr(mass), Hk, S, int(recent),
+                                       int(new_age), _ptr(slot), _stream(stream))
+    _check(st, "moda_depth_cache_admit")
+    return slot
 
 
 def moda_kv_proj_write(x: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor, kd: torch.Tensor,

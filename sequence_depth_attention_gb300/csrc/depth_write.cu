@@ -16,9 +16,20 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// slot_dev (may be null): the slot is read from device memory, as chosen by a
+// kernel earlier on the stream; one outside [0, L) writes nothing and latches
+// MODA_ERR_INVALID_ARG in the device error word.
 __global__ void __launch_bounds__(kThreads)
 depth_write_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int T, int Hk, int L,
-                   int slot, int lg_vpr, int64_t total_vec) {
+                   int slot, const int* __restrict__ slot_dev, unsigned int* err, int lg_vpr,
+                   int64_t total_vec) {
+  if (slot_dev) {
+    slot = *slot_dev;
+    if (slot < 0 || slot >= L) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(err, 0u, (unsigned int)MODA_ERR_INVALID_ARG);
+      return;
+    }
+  }
   const int vpr = 1 << lg_vpr;
   for (int64_t n = (int64_t)blockIdx.x * kThreads + threadIdx.x; n < total_vec;
        n += (int64_t)gridDim.x * kThreads) {
@@ -33,14 +44,15 @@ depth_write_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int T
 }  // namespace
 
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
-                               int num_sms, cudaStream_t stream) {
+                               const int* slot_dev, unsigned int* err, int num_sms,
+                               cudaStream_t stream) {
   const int lg_vpr = d == 128 ? 4 : 3;
   const int64_t total = (int64_t)T * Hk << lg_vpr;
   int64_t blocks = (total + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
   if (blocks > cap) blocks = cap;
   depth_write_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(
-      (const uint4*)src, (uint4*)dst, T, Hk, L, slot, lg_vpr, total);
+      (const uint4*)src, (uint4*)dst, T, Hk, L, slot, slot_dev, err, lg_vpr, total);
   return cudaGetLastError();
 }
 

@@ -202,8 +202,100 @@ moda_status moda_depth_write(const void* src, void* dst, int T, int Hk, int d, i
   unsigned int* err;
   moda_status st = device_state(&dev, &err, &sms);
   if (st != MODA_OK) return st;
-  cudaError_t e = moda::launch_depth_write(src, dst, T, Hk, d, L, slot, sms, (cudaStream_t)stream);
+  cudaError_t e = moda::launch_depth_write(src, dst, T, Hk, d, L, slot, nullptr, err, sms,
+                                           (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "depth_write launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_depth_write_at(const void* src, void* dst, int T, int Hk, int d, int L,
+                                const int* slot, moda_stream_t stream) {
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (Hk < 1) return fail(MODA_ERR_INVALID_ARG, "Hk = %d < 1", Hk);
+  if (L < 1) return fail(MODA_ERR_INVALID_ARG, "L = %d < 1", L);
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  if (!src || !dst || !slot) return fail(MODA_ERR_INVALID_ARG, "NULL src, dst or slot");
+  if (!aligned16(src) || !aligned16(dst))
+    return fail(MODA_ERR_MISALIGNED, "src or dst not 16-byte aligned");
+  if (((uintptr_t)slot & 3u) != 0) return fail(MODA_ERR_MISALIGNED, "slot not 4-byte aligned");
+  if (overlaps(src, (size_t)T * Hk * d * 2, dst, (size_t)Hk * T * L * d * 2))
+    return fail(MODA_ERR_INVALID_ARG, "src and dst overlap");
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_depth_write(src, dst, T, Hk, d, L, 0, slot, err, sms,
+                                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "depth_write launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+size_t moda_depth_mass_workspace_bytes(int T, int Hk, int L) {
+  if (T < 1 || Hk < 1 || L < 1) return 0;
+  return moda::depth_mass_workspace_floats(T, Hk, L) * sizeof(float);
+}
+
+moda_status moda_depth_mass(const void* q, const void* kd, const float* lse, int T, int Hq,
+                            int Hk, int d, int L, float scale, float* mass, float* workspace,
+                            size_t workspace_bytes, moda_stream_t stream) {
+  if (!q || !kd || !lse || !mass || !workspace)
+    return fail(MODA_ERR_INVALID_ARG, "NULL input, output or workspace pointer");
+  if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (L < 1) return fail(MODA_ERR_INVALID_ARG, "L = %d < 1", L);
+  if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
+  if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
+  if (!(scale > 0.f) || scale == __builtin_inff())
+    return fail(MODA_ERR_INVALID_ARG, "scale must be positive and finite");
+  const int G = Hq / Hk;
+  if (d != 64 && d != 128) return fail(MODA_ERR_UNSUPPORTED, "d = %d (supported: 64, 128)", d);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
+  if (T > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "T = %d > 2^24", T);
+  if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
+  const size_t need = moda::depth_mass_workspace_floats(T, Hk, L) * sizeof(float);
+  if (workspace_bytes < need)
+    return fail(MODA_ERR_INVALID_ARG, "workspace of %zu bytes; %zu needed", workspace_bytes, need);
+  if (!aligned16(q) || !aligned16(kd) || !aligned16(lse) || !aligned16(mass) || !aligned16(workspace))
+    return fail(MODA_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  const size_t mb = (size_t)Hk * L * 4;
+  const void* ins[3] = {q, kd, lse};
+  const size_t insz[3] = {(size_t)T * Hq * d * 2, (size_t)Hk * T * L * d * 2, (size_t)T * Hq * 4};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(mass, mb, ins[i], insz[i]) || overlaps(workspace, need, ins[i], insz[i]))
+      return fail(MODA_ERR_INVALID_ARG, "the output or the workspace overlaps an input");
+  if (overlaps(mass, mb, workspace, need))
+    return fail(MODA_ERR_INVALID_ARG, "mass and workspace overlap");
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  moda::DepthMassArgs a{q, kd, lse, T, Hq, Hk, d, L, G, scale, mass, workspace};
+  cudaError_t e = moda::launch_depth_mass(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "depth_mass launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_depth_cache_admit(int* slot_age, const float* mass, int Hk, int S, int recent,
+                                   int new_age, int* slot, moda_stream_t stream) {
+  if (!slot_age || !mass || !slot) return fail(MODA_ERR_INVALID_ARG, "NULL pointer");
+  if (S < 1) return fail(MODA_ERR_INVALID_ARG, "S = %d < 1", S);
+  if (Hk < 1) return fail(MODA_ERR_INVALID_ARG, "Hk = %d < 1", Hk);
+  if (recent < 0) return fail(MODA_ERR_INVALID_ARG, "recent = %d < 0", recent);
+  if (new_age < 0) return fail(MODA_ERR_INVALID_ARG, "new_age = %d < 0", new_age);
+  if (S > 1024) return fail(MODA_ERR_UNSUPPORTED, "S = %d > 1024", S);
+  if (((uintptr_t)slot_age & 3u) || ((uintptr_t)mass & 3u) || ((uintptr_t)slot & 3u))
+    return fail(MODA_ERR_MISALIGNED, "a pointer is not 4-byte aligned");
+  if (overlaps(slot_age, (size_t)S * 4, slot, 4) || overlaps(mass, (size_t)Hk * S * 4, slot, 4) ||
+      overlaps(slot_age, (size_t)S * 4, mass, (size_t)Hk * S * 4))
+    return fail(MODA_ERR_INVALID_ARG, "slot_age, mass and slot must not overlap");
+  int dev, sms;
+  unsigned int* err;
+  moda_status st = device_state(&dev, &err, &sms);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_cache_admit(slot_age, mass, Hk, S, recent, new_age, slot,
+                                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "cache_admit launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -92,8 +92,25 @@ cudaError_t launch_bwd_dq_tc(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_tc(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_kv_proj(const KvProjArgs& a, cudaStream_t stream);
+// slot_dev non-null: the slot index is read from device memory (see
+// depth_write.cu); err is the device error word.
 cudaError_t launch_depth_write(const void* src, void* dst, int T, int Hk, int d, int L, int slot,
-                               int num_sms, cudaStream_t stream);
+                               const int* slot_dev, unsigned int* err, int num_sms,
+                               cudaStream_t stream);
+
+// Arguments of one depth-mass call after validation on the host.
+struct DepthMassArgs {
+  const void *q, *kd;  // q [T,Hq,d]; kd packed [Hk,T,L,d] (bf16)
+  const float* lse;    // [T,Hq], natural log, from moda_fwd
+  int T, Hq, Hk, d, L, G;
+  float scale;
+  float* mass;         // [Hk, L] output
+  float* work;         // depth_mass_workspace_floats(T, Hk, L) floats
+};
+size_t depth_mass_workspace_floats(int T, int Hk, int L);
+cudaError_t launch_depth_mass(const DepthMassArgs& a, cudaStream_t stream);
+cudaError_t launch_cache_admit(int* ages, const float* mass, int Hk, int S, int recent,
+                               int new_age, int* slot_out, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* err, int timeout_ms, cudaStream_t stream);
 
 }  // namespace moda

@@ -199,3 +199,50 @@ def _dec(lib, q=A, kc=B, vc=C, kt=D, vt=E, stride=4 * 64, T=100, Hq=4, Hk=2, d=6
 ])
 def test_decode_rejects(lib, kw, code):
     assert _dec(lib, **kw) == code
+
+
+# ---- bounded depth cache entry points
+def test_depth_mass_workspace_formula(lib):
+    # one [L] partial per KV head and block of 64 positions
+    assert lib.moda_depth_mass_workspace_bytes(64, 4, 48) == 1 * 4 * 48 * 4
+    assert lib.moda_depth_mass_workspace_bytes(65536, 4, 48) == 1024 * 4 * 48 * 4
+    assert lib.moda_depth_mass_workspace_bytes(65, 2, 3) == 2 * 2 * 3 * 4
+    assert lib.moda_depth_mass_workspace_bytes(0, 4, 48) == 0
+
+
+def _mass(lib, q=A, kd=B, lse=C, T=100, Hq=4, Hk=2, d=64, L=4, scale=0.125, mass=D, ws=E,
+          wsb=1 << 20):
+    return lib.moda_depth_mass(q, kd, lse, T, Hq, Hk, d, L, scale, mass, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(ws=None), INVALID), (dict(T=0), INVALID), (dict(L=0), INVALID),
+    (dict(Hq=5, Hk=2), INVALID), (dict(scale=0.0), INVALID), (dict(wsb=16), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(Hq=6, Hk=2), UNSUPPORTED), (dict(L=1025), UNSUPPORTED),
+    (dict(lse=C + 4), MISALIGNED), (dict(mass=A), INVALID), (dict(ws=C), INVALID),
+])
+def test_depth_mass_rejects(lib, kw, code):
+    assert _mass(lib, **kw) == code
+
+
+def _admit(lib, ages=A, mass=B, Hk=2, S=4, recent=1, new_age=5, slot=C):
+    return lib.moda_depth_cache_admit(ages, mass, Hk, S, recent, new_age, slot, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ages=None), INVALID), (dict(slot=None), INVALID), (dict(S=0), INVALID),
+    (dict(Hk=0), INVALID), (dict(recent=-1), INVALID), (dict(new_age=-1), INVALID),
+    (dict(S=1025), UNSUPPORTED), (dict(slot=C + 2), MISALIGNED), (dict(slot=A + 4), INVALID),
+])
+def test_cache_admit_rejects(lib, kw, code):
+    assert _admit(lib, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((A, B, 0, 2, 64, 4, C), INVALID), ((A, B, 8, 2, 64, 0, C), INVALID),
+    ((A, B, 8, 2, 64, 4, None), INVALID), ((A, B, 8, 2, 96, 4, C), UNSUPPORTED),
+    ((A, B, 8, 2, 64, 2000, C), UNSUPPORTED), ((A + 8, B, 8, 2, 64, 4, C), MISALIGNED),
+    ((A, B, 8, 2, 64, 4, C + 1), MISALIGNED), ((A, A + 256, 8, 2, 64, 4, C), INVALID),
+])
+def test_depth_write_at_rejects(lib, args, code):
+    assert lib.moda_depth_write_at(*args, None) == code
