@@ -1,6 +1,7 @@
 // MoDA forward on the 5th-generation tensor core (sm_103a): TMA-staged tiles,
-// tcgen05.mma into tensor memory (TMEM), warp-specialised pipeline. This
-// kernel serves d = 128; d = 64 runs two tiles per CTA (fwd_pp.cu).
+// tcgen05.mma into tensor memory (TMEM), warp-specialised pipeline, one
+// persistent CTA per SM. This kernel serves d = 128; d = 64 runs two tiles per
+// CTA (fwd_pp.cu).
 //
 // What it computes is Mixture-of-Depths Attention, Sec. 2.2 (one softmax over
 // the causal sequence keys of the layer and the L depth slots of the same
@@ -12,32 +13,43 @@
 //     q[T][Hq][d] lands exactly this stacking, so every K/V block staged in
 //     shared memory serves all G heads;
 //   * depth blocks: the packed depth rows of the tile's positions are one
-//     contiguous run kd[hk][p0 .. p0+128/G)[0..L) (chunk-aware layout), read
-//     128 rows per block; row r keeps depth column j iff floor(j/L) == r/G
-//     (block-diagonal mask of Sec. 3.3). An exact online softmax does not
-//     depend on block order, so depth blocks are spread evenly among the
-//     sequence blocks: each tile streams its depth rows from HBM over its
-//     lifetime instead of all CTAs of a wave reading them at once;
+//     contiguous run kd[hk][p0 .. p0+128/G)[0..L) (chunk-aware layout). Each
+//     softmax warp owns one 32-row word of every depth block, filled with the
+//     next packed rows of its own positions, so a row keeps depth columns of
+//     its own warp's word only (the block-diagonal mask of Sec. 3.3 within
+//     that word). An exact online softmax does not depend on block order, so
+//     depth blocks are spread evenly among the sequence blocks: each tile
+//     streams its depth rows from HBM over its lifetime;
 //   * sequence blocks of 128 keys, the grouped causal mask key <= p0 + r/G
 //     applied only on blocks that reach past p0;
 //   * one running state per row: max m (log2 units), sum l, and the
 //     unnormalised output O, which lives in TMEM and is accumulated by the
 //     tensor core; o = O / l once at the end, lse = m ln2 + ln l.
 //
-// Roles (8 warps, one CTA per tile; KV-head-major, longest tiles first):
-//   warp 0  lane 0: TMA producer for Q and the K blocks
+// Persistent CTAs: the grid is one CTA per SM, and each CTA takes tiles from
+// a queue in global memory (KV-head-major, longest tiles first within a head,
+// as the hardware would dispatch one CTA per tile). The pipeline runs on
+// across tile boundaries: the next tile's Q and K/V blocks load while the
+// current one finishes, its first S = Q K^T products run during the current
+// tile's last block and epilogue, so a tile costs no launch, prologue or
+// pipeline drain. The K-producer warp takes tiles from the queue and passes
+// their numbers to the other roles through a ring in shared memory.
+//
+// Roles (8 warps):
+//   warp 0  lane 0: tile queue, TMA producer for Q and the K blocks
 //   warp 1  lane 0: tcgen05.mma issuer of S = Q K^T; the whole warp allocates TMEM
 //   warp 2  lane 0: TMA producer for the V blocks
 //   warp 3  lane 0: tcgen05.mma issuer of O += P V
-//   warps 4-7     : softmax, one thread per tile row (= TMEM lane), and the
-//                   epilogue
+//   warps 4-7     : softmax, one thread per tile row (= TMEM lane), the copy
+//                   of each tile's Q into TMEM, and the epilogue
 // TMEM (512 columns): S double buffer [0,128) [128,256), O [256, 256+d),
 // P (bf16 pairs) [384,448), Q (bf16 pairs) [448, 448+d/2). The softmax warps
-// copy the tile's Q rows from shared memory into TMEM once, so S = Q K^T
-// reads only K from shared memory (an MMA with both operands in shared memory
-// would use the whole shared-memory read bandwidth and starve the TMA writes
-// of the next K/V blocks). The MMA computes S_{j+1} = Q K_{j+1}^T while the
-// softmax turns S_j into P_j, then O += P_j V_j with P read straight from TMEM.
+// copy each tile's Q rows from shared memory into TMEM once the previous
+// tile's last S = Q K^T has completed, so S reads only K from shared memory
+// (an MMA with both operands in shared memory would use the whole
+// shared-memory read bandwidth and starve the TMA writes of the next K/V
+// blocks). The MMA computes S_{j+1} = Q K_{j+1}^T while the softmax turns S_j
+// into P_j, then O += P_j V_j with P read straight from TMEM.
 // The running max is rescaled lazily: O and l are rescaled only when a new
 // block raises the row max by more than 8 (a factor 256), which stays exact
 // because o = O / l uses the same reference for both.
@@ -64,16 +76,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kSumBound = 256.0f;         // 2^kRescaleThreshold
+constexpr int kTileRing = 4;                // tile numbers in flight between roles
+// arrivals that free a tile-ring entry: V producer, S issuer, P.V issuer, 4 softmax warps
+constexpr int kTileReaders = 7;
 
 template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;     // 64-column (128-byte) swizzle boxes per row
   static constexpr int kBoxBytes = 128 * 64 * 2;
   static_assert(D == 128, "d = 64 runs the two-tile kernel (fwd_pp.cu)");
-  static constexpr int kNSK = 3;  // K stages in the K region
+  static constexpr int kNSK = 3;  // K stages
   static constexpr int kNSV = 3;  // V stages
-  // one more K stage lives in the Q region once Q has been copied to TMEM
-  static constexpr int kNSKT = kNSK + 1;
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kOffQ = 0;
@@ -86,29 +99,81 @@ struct Cfg {
 };
 
 struct alignas(8) Barriers {
-  uint64_t q_full;
-  uint64_t k_full[8], k_empty[8];
-  uint64_t v_full[8], v_empty[8];
+  uint64_t q_full, q_tmem;  // Q of the current tile landed / copied into TMEM
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t q_tmem;
+  uint64_t t_full[kTileRing], t_empty[kTileRing];
   uint64_t mma_done, mma_done_pv;
+  int tile_ring[kTileRing];
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Params {
-  int T, Hq, Hk, L, lgG, ntiles;
+  int T, Hq, Hk, L, lgG, ntiles, total;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
+  unsigned int* queue;  // {next tile, CTAs finished}
 };
 
 // All lanes poll; the warp proceeds only if every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Geometry of one tile (queue entry o: KV-head-major, longest tiles first).
+struct Tile {
+  int hk, p0, npos, t_last, PW, RW, n_depth, nb, depth_row0;
+  __device__ void set(int o, const Params& p) {
+    const int P = BM >> p.lgG;  // positions per tile
+    const int tile = p.ntiles - 1 - o % p.ntiles;
+    hk = o / p.ntiles;
+    p0 = tile * P;
+    npos = min(P, p.T - p0);
+    t_last = p0 + npos - 1;
+    PW = P >> 2;                     // positions per softmax warp
+    RW = PW * p.L;                   // packed depth rows per softmax warp
+    n_depth = (min(npos, PW) * p.L + 31) / 32;
+    nb = n_depth + t_last / BN + 1;
+    depth_row0 = (hk * p.T + p0) * p.L;
+  }
+};
+
+// Block schedule of a tile: the n_depth depth blocks are spread evenly among
+// the sequence blocks (Bresenham: block j is a depth block iff
+// floor((j+1)*n_depth/nb) > floor(j*n_depth/nb)). Every role walks the blocks
+// in order with its own copy.
+struct Sched {
+  int acc = 0, db = 0, sbk = 0;  // remainder, depth blocks so far, sequence blocks so far
+  bool depth = false;            // is the current block a depth block
+  int index = 0;                 // its index among blocks of its kind
+  __device__ void next(int n_depth, int nb) {
+    acc += n_depth;
+    depth = acc >= nb;
+    if (depth) {
+      acc -= nb;
+      index = db++;
+    } else {
+      index = sbk++;
+    }
+  }
+};
+
+// The k-th tile of this CTA from the ring (-1: no more tiles); the reader
+// frees the entry right away. False on a timeout.
+__device__ __forceinline__ bool read_tile(Barriers* bars, int k, volatile int* abort, int* o,
+                                          bool arrive) {
+  const int s = k % kTileRing;
+  if (!warp_wait(smem_u32(&bars->t_full[s]), (k / kTileRing) & 1, abort)) return false;
+  *o = *reinterpret_cast<volatile int*>(&bars->tile_ring[s]);
+  __syncwarp();
+  if (arrive) mbar_arrive(smem_u32(&bars->t_empty[s]));
+  return true;
 }
 
 // p = 2^(s*sl - m) for the N raw scores x (fp32 bits) as bf16 pairs into pk;
@@ -179,51 +244,12 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = 1 << p.lgG;
-  const int P = BM >> p.lgG;  // positions per tile
-  // KV-head-major grid, longest tiles first within a head: the CTAs resident
-  // at one time share one or two heads' K/V, which then stay in L2 while the
-  // tiles stream through them (head-interleaved, they span every head's K/V)
-  const int tile = p.ntiles - 1 - (int)(blockIdx.x % p.ntiles);
-  const int hk = (int)(blockIdx.x / p.ntiles);
-  const int p0 = tile * P;
-  const int npos = min(P, p.T - p0);
-  const int t_last = p0 + npos - 1;
-  // Depth blocks, one 32-row word per softmax warp: warp w (rows 32w..32w+31,
-  // positions p0 + w*PW .. + PW) owns columns [32w, 32w+32) of every depth
-  // block, filled with the next 32 of its own RW = PW*L packed depth rows.
-  // Each row's slots then fall in its own warp's word, so a softmax warp
-  // exponentiates 32 columns of a depth block instead of 128; the tensor core
-  // still computes the whole block (the other words of a row are masked).
-  const int PW = P >> 2;                 // positions per softmax warp
-  const int RW = PW * p.L;               // packed depth rows per warp
-  const int n_depth = (min(npos, PW) * p.L + 31) / 32;
-  const int nb = n_depth + t_last / BN + 1;
-  const int depth_row0 = (hk * p.T + p0) * p.L;  // first packed depth row of the tile
-  // Block schedule: the n_depth depth blocks are spread evenly among the
-  // sequence blocks (Bresenham: block j is a depth block iff
-  // floor((j+1)*n_depth/nb) > floor(j*n_depth/nb)), so each tile streams its
-  // depth rows from HBM over its whole lifetime instead of in one burst.
-  // Every role walks the blocks in order with its own Sched copy.
-  struct Sched {
-    int acc = 0, db = 0, sbk = 0;  // remainder, depth blocks so far, sequence blocks so far
-    bool depth = false;            // is the current block a depth block
-    int index = 0;                 // its index among blocks of its kind
-    __device__ void next(int n_depth, int nb) {
-      acc += n_depth;
-      depth = acc >= nb;
-      if (depth) {
-        acc -= nb;
-        index = db++;
-      } else {
-        index = sbk++;
-      }
-    }
-  };
 
   if (tid == 0) {
     bars->abort = 0;
     mbar_init(smem_u32(&bars->q_full), 1);
-    for (int s = 0; s < 8; ++s) {
+    mbar_init(smem_u32(&bars->q_tmem), 128);
+    for (int s = 0; s < 4; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
       mbar_init(smem_u32(&bars->k_empty[s]), 1);
       mbar_init(smem_u32(&bars->v_full[s]), 1);
@@ -235,9 +261,12 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(smem_u32(&bars->p_full[b]), 128);
       mbar_init(smem_u32(&bars->pv_done[b]), 1);
     }
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(smem_u32(&bars->t_full[s]), 1);
+      mbar_init(smem_u32(&bars->t_empty[s]), kTileReaders);
+    }
     mbar_init(smem_u32(&bars->mma_done), 1);
     mbar_init(smem_u32(&bars->mma_done_pv), 1);
-    mbar_init(smem_u32(&bars->q_tmem), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -261,10 +290,11 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------ TMA producers
     // The whole warp runs the loop (uniform control flow); one elected lane
-    // issues the copies.
+    // issues the copies. Stages and phases follow the CTA's running block
+    // count g across tiles.
     const bool leader = elect_one();
     const bool is_k = warp == 0;
-    const int NS = is_k ? C::kNSKT : C::kNSV;
+    const int NS = is_k ? C::kNSK : C::kNSV;
     const uint32_t sbase = is_k ? sK : sV;
     const CUtensorMap* seq_map = is_k ? &tmK : &tmV;
     const CUtensorMap* dep_map = is_k ? &tmKd : &tmVd;
@@ -274,47 +304,74 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // push the K/V blocks that later tiles of the head re-read out of L2
     // (K/V keep the default policy; pinning all of them measured slower).
     const uint64_t pol_once = l2_policy_evict_first();
-    if (is_k && leader) {
-      const uint32_t qb = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qb, C::kQBytes);
-      for (int c = 0; c < C::kBoxes; ++c)
-        tma_load_3d_hint(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, hk * G, p0, pol_once);
-    }
-    int issued = 0;
-    Sched sch;
-    for (int j = 0; j < nb; ++j) {
-      sch.next(n_depth, nb);
-      const int s = j % NS;
-      const bool ok = mbar_wait_bounded(smem_u32(&empty[s]), ((j / NS) & 1) ^ 1, abort, kTimeoutNs);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      // the K stage in the Q region is first written once Q sits in TMEM
-      if (is_k && j == C::kNSK && !warp_wait(smem_u32(&bars->q_tmem), 0, abort)) break;
-      if (leader) {
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, C::kKVBytes);
-        const uint32_t dst = (is_k && s == C::kNSK) ? sQ : sbase + s * C::kKVBytes;
-        if (sch.depth) {
-          // four 32-row words: rows [32w, 32w+32) of the stage hold warp w's
-          // packed depth rows 32*index .. +32 (128-byte swizzle atoms are 8
-          // rows, so a word starts on an atom boundary)
-          for (int w = 0; w < 4; ++w)
-            for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_2d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64,
-                               depth_row0 + w * RW + sch.index * 32, pol_once);
-        } else {
-          for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, hk, sch.index * BN);
+    int g = 0;   // blocks issued so far, over all tiles
+    int nq = 0;  // Q loads issued
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int o;
+      if (is_k) {
+        // take the next tile from the queue and pass it on
+        const int s = k % kTileRing;
+        if (!warp_wait(smem_u32(&bars->t_empty[s]), ((k / kTileRing) & 1) ^ 1, abort)) break;
+        if (leader) {
+          const unsigned int t = atomicAdd(p.queue, 1u);
+          o = t < (unsigned int)p.total ? (int)t : -1;
+          *reinterpret_cast<volatile int*>(&bars->tile_ring[s]) = o;
+          mbar_arrive(smem_u32(&bars->t_full[s]));
         }
+        o = __shfl_sync(0xffffffffu, o, __ffs(__ballot_sync(0xffffffffu, leader)) - 1);
+      } else if (!read_tile(bars, k, abort, &o, leader)) {
+        break;
       }
-      __syncwarp();
-      issued = j + 1;
+      if (o < 0) break;
+      Tile tl;
+      tl.set(o, p);
+      if (is_k) {
+        // Q of this tile, once the softmax warps have copied the previous Q
+        // into TMEM (the Q region is free again)
+        if (k > 0 && !warp_wait(smem_u32(&bars->q_tmem), (k - 1) & 1, abort)) break;
+        if (leader) {
+          const uint32_t qb = smem_u32(&bars->q_full);
+          mbar_arrive_expect_tx(qb, C::kQBytes);
+          for (int c = 0; c < C::kBoxes; ++c)
+            tma_load_3d_hint(sQ + c * C::kBoxBytes, &tmQ, qb, c * 64, tl.hk * G, tl.p0, pol_once);
+        }
+        ++nq;
+      }
+      Sched sch;
+      for (int j = 0; j < tl.nb; ++j, ++g) {
+        sch.next(tl.n_depth, tl.nb);
+        const int s = g % NS;
+        if (!warp_wait(smem_u32(&empty[s]), ((g / NS) & 1) ^ 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, C::kKVBytes);
+          const uint32_t dst = sbase + s * C::kKVBytes;
+          if (sch.depth) {
+            // four 32-row words: rows [32w, 32w+32) of the stage hold warp w's
+            // packed depth rows 32*index .. +32 (128-byte swizzle atoms are 8
+            // rows, so a word starts on an atom boundary)
+            for (int w = 0; w < 4; ++w)
+              for (int c = 0; c < C::kBoxes; ++c)
+                tma_load_2d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64,
+                                 tl.depth_row0 + w * tl.RW + sch.index * 32, pol_once);
+          } else {
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, tl.hk, sch.index * BN);
+          }
+        }
+        __syncwarp();
+      }
     }
     // drain: every copy this warp issued has landed before smem is released
     if (leader) {
       int never = 0;
-      for (int j = max(0, issued - NS); j < issued; ++j)
+      for (int j = max(0, g - NS); j < g; ++j)
         mbar_wait_bounded(smem_u32(&full[j % NS]), (j / NS) & 1, &never, kTimeoutNs);
-      if (is_k) mbar_wait_bounded(smem_u32(&bars->q_full), 0, &never, kTimeoutNs);
+      if (is_k && nq > 0) mbar_wait_bounded(smem_u32(&bars->q_full), (nq - 1) & 1, &never, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 3) {
@@ -329,57 +386,82 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
       };
+      auto next_tile = [&](int k, int* o) -> bool {
+        const int s = k % kTileRing;
+        if (!wait(&bars->t_full[s], (k / kTileRing) & 1)) return false;
+        *o = *reinterpret_cast<volatile int*>(&bars->tile_ring[s]);
+        mbar_arrive(smem_u32(&bars->t_empty[s]));
+        return true;
+      };
       // all descriptors here share the high word (SBO 1024, 128-byte swizzle);
       // tile offsets are 32-bit adds to the start address field of the low word
       const uint64_t dk = sdesc_sw128(sK, 16, 1024);
       const uint32_t hi = (uint32_t)(dk >> 32);
+      int g = 0;  // blocks issued so far, over all tiles
       if (warp == 1) {
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
-        const uint32_t k_lo = (uint32_t)dk, q_lo = (uint32_t)sdesc_sw128(sQ, 16, 1024);
-        // S_j = Q K_j^T into S buffer j&1 (K stage already waited for)
-        auto issue_s = [&](int j) {
-          const int s = j % C::kNSKT;
-          const uint32_t ks = s == C::kNSK ? q_lo : k_lo + ((uint32_t)(s * C::kKVBytes) >> 4);
-          const uint32_t dcol = tbase + C::kColS + (j & 1) * 128;
+        const uint32_t k_lo = (uint32_t)dk;
+        // S_g = Q K_g^T into S buffer g&1 as soon as the softmax has read
+        // S_{g-2} out of that buffer and K_g has landed: S_{g+2} runs on the
+        // tensor core while the softmax works on g. A tile's first S also
+        // waits until the tile's Q sits in TMEM.
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          int o;
+          if (!next_tile(k, &o) || o < 0) break;
+          Tile tl;
+          tl.set(o, p);
+          if (!wait(&bars->q_tmem, k & 1)) break;
+          for (int j = 0; j < tl.nb; ++j, ++g) {
+            const int ks = g % C::kNSK;
+            if (g >= 2 && !wait(&bars->s_free[g & 1], ((g - 2) >> 1) & 1)) {
+              ok = false;
+              break;
+            }
+            if (!wait(&bars->k_full[ks], (g / C::kNSK) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kb = k_lo + ((uint32_t)(ks * C::kKVBytes) >> 4);
+            const uint32_t dcol = tbase + C::kColS + (g & 1) * 128;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ts(dcol, tbase + C::kColQ + kk * 8, desc_join(ks + off, hi), idS, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+              mma_ts(dcol, tbase + C::kColQ + kk * 8, desc_join(kb + off, hi), idS, kk > 0);
+            }
+            tc_commit(smem_u32(&bars->k_empty[ks]));
+            tc_commit(smem_u32(&bars->s_full[g & 1]));
           }
-          tc_commit(smem_u32(&bars->k_empty[s]));
-          tc_commit(smem_u32(&bars->s_full[j & 1]));
-        };
-        // S_0, S_1, then S_{j+2} as soon as the softmax has read S_j out of
-        // its buffer: S_{j+2} runs on the tensor core while the softmax works on j
-        bool ok = wait(&bars->q_tmem, 0) && wait(&bars->k_full[0], 0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-        }
-        for (int j = 1; ok && j < nb; ++j) {
-          const int ks = j % C::kNSKT;
-          if (j >= 2 && !wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1)) break;
-          if (!wait(&bars->k_full[ks], (j / C::kNSKT) & 1)) break;
-          tc_fence_after();
-          issue_s(j);
         }
       } else {
         constexpr uint32_t idPV = idesc_bf16_f32(BM, D, true);
         const uint32_t v_lo = (uint32_t)sdesc_sw128(sV, C::kBoxBytes, 1024);
         const uint32_t pcol = tbase + C::kColP;
-        for (int j = 0; j < nb; ++j) {
-          const int sb = j & 1, vs = j % C::kNSV;
-          if (!wait(&bars->p_full[sb], (j >> 1) & 1)) break;
-          if (!wait(&bars->v_full[vs], (j / C::kNSV) & 1)) break;
-          tc_fence_after();
-          const uint32_t vb = v_lo + ((uint32_t)(vs * C::kKVBytes) >> 4);
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          int o;
+          if (!next_tile(k, &o) || o < 0) break;
+          Tile tl;
+          tl.set(o, p);
+          for (int j = 0; j < tl.nb; ++j, ++g) {
+            const int sb = g & 1, vs = g % C::kNSV;
+            if (!wait(&bars->p_full[sb], (g >> 1) & 1) || !wait(&bars->v_full[vs], (g / C::kNSV) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vb = v_lo + ((uint32_t)(vs * C::kKVBytes) >> 4);
+            // a tile's first P.V overwrites O (the softmax warps have read the
+            // previous tile's O before they stored this P)
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + C::kColO, pcol + kk * 8, desc_join(vb + ((uint32_t)(kk * 2048) >> 4), hi), idPV,
-                   kk > 0 ? 1u : acc0);
-          tc_commit(smem_u32(&bars->v_empty[vs]));
-          tc_commit(smem_u32(&bars->pv_done[sb]));
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tbase + C::kColO, pcol + kk * 8, desc_join(vb + ((uint32_t)(kk * 2048) >> 4), hi),
+                     idPV, kk > 0 ? 1u : acc0);
+            tc_commit(smem_u32(&bars->v_empty[vs]));
+            tc_commit(smem_u32(&bars->pv_done[sb]));
+          }
         }
       }
       // every MMA issued by this thread has completed before TMEM is freed
@@ -393,202 +475,227 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // ------------------------------------------------------ softmax + epilogue
     const int row = tid - 128;                 // tile row == TMEM lane
     const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
-    const int lp = row >> p.lgG;
-    const int t_row = p0 + lp;
-    const int h_row = hk * G + (row & (G - 1));
-    const bool valid = t_row < p.T;
-    const int t_mask = min(t_row, p.T - 1);
     const int wq = warp & 3;                    // this warp's word of a depth block
-    const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's RW rows
-    const int dw_n = valid ? p.L : 0;            // rows past T keep no depth column
+    const int lp = row >> p.lgG;
+    const int h_off = row & (G - 1);
     const float sl = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t zeros[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    bool p_zero = false;  // this warp's P columns outside its depth word hold zeros
+    int g = 0;            // blocks processed so far, over all tiles
     bool ok = true;
-    // Q row -> TMEM columns [kColQ, kColQ + d/2) as bf16 pairs in row order, the
-    // A operand of S = Q K^T (so the MMA reads only K from shared memory)
-    if (!warp_wait(smem_u32(&bars->q_full), 0, abort)) ok = false;
-    if (ok) {
+    // Q of tile k (landed in shared memory) -> TMEM columns [kColQ, kColQ + d/2)
+    // as bf16 pairs in row order, the A operand of S = Q K^T. Called once
+    // every S product of the previous tile has completed.
+    auto copy_q = [&](int k) -> bool {
+      if (!warp_wait(smem_u32(&bars->q_full), k & 1, abort)) return false;
       const uint8_t* qrow = smem + C::kOffQ + row * 128;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * C::kBoxBytes + ((k ^ (row & 7)) << 4));
-          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * C::kBoxBytes + ((i ^ (row & 7)) << 4));
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
         tmem_st32(tmem_addr(tbase, lane_base, C::kColQ + c * 32), w);
       }
       tmem_st_wait();
       tc_fence_before();
-      // the Q region becomes a K stage (TMA writes): order these reads first
+      // the Q region takes the next tile's Q (a TMA write): order these reads first
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(smem_u32(&bars->q_tmem));
-    }
-    // Rescale O and l to a new reference when a block's raw max mx (log2
-    // units) rose more than the threshold above it; false on a timeout.
-    auto rescale = [&](float mx, int j) -> bool {
-      const bool need = mx > m_ref + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mx : m_ref;
-        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-        if (j > 0) {
-          // O holds blocks 0..j-1: wait for the last of them, then rescale it
-          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
-            tmem_ld32(ta, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(ta, r);
-          }
-          tmem_st_wait();
-        }
-        l *= alpha;
-        m_ref = m_new;
-      }
       return true;
     };
-    // Fast path of every block: exponentiate against the running reference
-    // m_ref right away. Every p is at most the block's sum, so a sum within
-    // 2^threshold proves no score rose more than the threshold above m_ref,
-    // and the block needs no max at all. Only if some row of the warp has no
-    // reference yet, or its sum exceeds the bound, fall back to max-first with
-    // a rescale of O and l where the max really rose that far.
-    const uint32_t zeros[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    bool p_zero = false;  // this warp's P columns outside its depth word hold zeros
-    Sched sch;
-    for (int j = 0; ok && j < nb; ++j) {
-      sch.next(n_depth, nb);
-      const int sb = j & 1;
-      if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort)) {
+    int o_cur;
+    ok = read_tile(bars, 0, abort, &o_cur, lane == 0);
+    if (ok && o_cur >= 0) ok = copy_q(0);
+    for (int k = 0; ok && o_cur >= 0; ++k) {
+      Tile tl;
+      tl.set(o_cur, p);
+      // After the tile's last block (its S has been read, so every S product
+      // that used this tile's Q has completed), the next tile's number is
+      // read from the ring (the K producer publishes it after this tile's
+      // last K load) and its Q goes into TMEM, so that its first S products
+      // run while this tile's last P.V completes and its epilogue runs.
+      int o_next = -1;
+      auto prepare_next = [&]() -> bool {
+        if (!read_tile(bars, k + 1, abort, &o_next, lane == 0)) return false;
+        return o_next < 0 || copy_q(k + 1);
+      };
+      const int t_row = tl.p0 + lp;
+      const int h_row = tl.hk * G + h_off;
+      const bool valid = t_row < p.T;
+      const int t_mask = min(t_row, p.T - 1);
+      const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's RW rows
+      const int dw_n = valid ? p.L : 0;             // rows past T keep no depth column
+      float m_ref = -INFINITY, l = 0.f;
+      // Rescale O and l to a new reference when a block's raw max mx (log2
+      // units) rose more than the threshold above it; false on a timeout.
+      // O holds this tile's blocks 0..j-1 (nothing of it when j == 0).
+      auto rescale = [&](float mx, int j) -> bool {
+        const bool need = mx > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mx : m_ref;
+          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+          if (j > 0) {
+            if (!warp_wait(smem_u32(&bars->pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              const uint32_t ta = tmem_addr(tbase, lane_base, C::kColO + c * 32);
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(ta, r);
+            }
+            tmem_st_wait();
+          }
+          l *= alpha;
+          m_ref = m_new;
+        }
+        return true;
+      };
+      // Fast path of every block: exponentiate against the running reference
+      // m_ref right away. Every p is at most the block's sum, so a sum within
+      // 2^threshold proves no score rose more than the threshold above m_ref,
+      // and the block needs no max at all. Only if some row of the warp has no
+      // reference yet, or its sum exceeds the bound, fall back to max-first
+      // with a rescale of O and l where the max really rose that far.
+      Sched sch;
+      for (int j = 0; j < tl.nb; ++j, ++g) {
+        sch.next(tl.n_depth, tl.nb);
+        const int sb = g & 1;
+        if (!warp_wait(smem_u32(&bars->s_full[sb]), (g >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pcol = tmem_addr(tbase, lane_base, C::kColP);
+        float sum = 0.f;
+        if (sch.depth) {
+          // depth block: only this warp's word of 32 columns can hold its rows'
+          // slots; mask (on raw scores, scale > 0) to the row's own slots with
+          // one validity word, a bit test and a select per column
+          uint32_t xs[32];
+          tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + wq * 32), xs);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars->s_free[sb]));
+          const int lo = dw_lo - sch.index * 32, hi = lo + dw_n;
+          const int a = min(max(lo, 0), 32), b = min(max(hi, 0), 32);
+          const uint32_t word =
+              (b >= 32 ? 0xffffffffu : (1u << b) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
+          uint32_t pk[16];
+          bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            sum = exp_block<32>(xs, pk, sl, m_ref);
+            slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
+          }
+          if (slow) {
+            if (!rescale(raw_max32(xs) * sl, j)) {
+              ok = false;
+              break;
+            }
+            sum = exp_block<32>(xs, pk, sl, m_ref);
+          }
+          l += sum;
+          // P_g overwrites P_{g-1}: the tensor core must have consumed it
+          if (g >= 1) {
+            if (!warp_wait(smem_u32(&bars->pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st16(pcol + wq * 16, pk);
+          if (!p_zero) {
+            for (int kk = 1; kk < 4; ++kk) tmem_st16(pcol + ((wq + kk) & 3) * 16, zeros);
+          }
+          p_zero = true;
+        } else {
+          // sequence block: S row of this thread, 128 raw fp32 scores as bits
+          uint32_t x[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
+          tmem_ld_wait();
+          // S_g is in registers: its TMEM buffer may take S_{g+2}
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars->s_free[sb]));
+          // the grouped causal mask keeps columns below hi (on raw scores:
+          // scale > 0, so masking and the max commute with scaling)
+          const int k0 = sch.index * BN;
+          if (k0 + BN - 1 > tl.p0) {
+            const int hi = t_mask - k0 + 1;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
+          }
+          uint32_t pk[BN / 2];
+          bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            sum = exp_block<BN>(x, pk, sl, m_ref);
+            slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
+          }
+          if (slow) {
+            if (!rescale(raw_max128(x) * sl, j)) {
+              ok = false;
+              break;
+            }
+            sum = exp_block<BN>(x, pk, sl, m_ref);
+          }
+          l += sum;
+          // P_g overwrites P_{g-1}: the tensor core must have consumed it (the
+          // slow path above may have waited for it already; the phase test is
+          // idempotent)
+          if (g >= 1) {
+            if (!warp_wait(smem_u32(&bars->pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) tmem_st32(pcol + c * 32, pk + c * 32);
+          p_zero = false;
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[sb]));
+      }
+      if (!ok || !prepare_next()) break;
+      // epilogue: O holds every block of the tile once the last P.V is done
+      // (commits complete in issue order)
+      if (!warp_wait(smem_u32(&bars->pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t pcol = tmem_addr(tbase, lane_base, C::kColP);
-      float sum = 0.f;
-      if (sch.depth) {
-        // depth block: only this warp's word of 32 columns can hold its rows'
-        // slots; mask (on raw scores, scale > 0) to the row's own slots with
-        // one validity word, a bit test and a select per column
-        uint32_t xs[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + wq * 32), xs);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->s_free[sb]));
-        const int lo = dw_lo - sch.index * 32, hi = lo + dw_n;
-        const int a = min(max(lo, 0), 32), b = min(max(hi, 0), 32);
-        const uint32_t word = (b >= 32 ? 0xffffffffu : (1u << b) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+      uint32_t r[D];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
-        uint32_t pk[16];
-        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
-        if (!slow) {
-          sum = exp_block<32>(xs, pk, sl, m_ref);
-          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
-        }
-        if (slow) {
-          if (!rescale(raw_max32(xs) * sl, j)) {
-            ok = false;
-            break;
-          }
-          sum = exp_block<32>(xs, pk, sl, m_ref);
-        }
-        l += sum;
-        // P_j overwrites P_{j-1}: the tensor core must have consumed it
-        if (j >= 1) {
-          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        tmem_st16(pcol + wq * 16, pk);
-        if (!p_zero) {
-          for (int k = 0; k < 4; ++k)
-            if (k != wq) tmem_st16(pcol + k * 16, zeros);
-        }
-        p_zero = true;
-      } else {
-        // sequence block: S row of this thread, 128 raw fp32 scores as bits
-        uint32_t x[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(tmem_addr(tbase, lane_base, C::kColS + sb * 128 + c * 32), x + c * 32);
-        tmem_ld_wait();
-        // S_j is in registers: its TMEM buffer may take S_{j+2}
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->s_free[sb]));
-        // the grouped causal mask keeps columns below hi (on raw scores:
-        // scale > 0, so masking and the max commute with scaling)
-        const int k0 = sch.index * BN;
-        if (k0 + BN - 1 > p0) {
-          const int hi = t_mask - k0 + 1;
-#pragma unroll
-          for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
-        }
-        uint32_t pk[BN / 2];
-        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
-        if (!slow) {
-          sum = exp_block<BN>(x, pk, sl, m_ref);
-          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
-        }
-        if (slow) {
-          if (!rescale(raw_max128(x) * sl, j)) {
-            ok = false;
-            break;
-          }
-          sum = exp_block<BN>(x, pk, sl, m_ref);
-        }
-        l += sum;
-        // P_j overwrites P_{j-1}: the tensor core must have consumed it (the
-        // slow path above may have waited for it already; the phase test is
-        // idempotent)
-        if (j >= 1) {
-          if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int c = 0; c < BN / 64; ++c) tmem_st32(pcol + c * 32, pk + c * 32);
-        p_zero = false;
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[sb]));
-    }
-    if (ok) {
-      ok = warp_wait(smem_u32(&bars->pv_done[(nb - 1) & 1]), ((nb - 1) >> 1) & 1, abort);
-      if (ok && nb >= 2)
-        ok = warp_wait(smem_u32(&bars->pv_done[(nb - 2) & 1]), ((nb - 2) >> 1) & 1, abort);
-    }
-    if (ok) {
-      tc_fence_after();
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::kColO + c * 32), r + c * 32);
+      tmem_ld_wait();
       const float inv = 1.f / l;
       __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
+      if (valid) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::kColO + c * 32), r);
-        tmem_ld_wait();
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * c]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
+          reinterpret_cast<uint4*>(orow)[c] = v;
         }
+        if (p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
       }
-      if (valid && p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
+      // O has been read: the next tile's first P.V may overwrite it (that
+      // P.V follows this warp's next p_full arrival, so program order suffices)
+      tc_fence_before();
+      o_cur = o_next;
     }
   }
 
@@ -598,7 +705,16 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  if (tid == 0 && bars->abort) atomicCAS(p.err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+  if (tid == 0) {
+    if (bars->abort) atomicCAS(p.err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+    // the last CTA to finish puts the queue back to zero for the next launch
+    __threadfence();
+    if (atomicAdd(p.queue + 1, 1u) == gridDim.x - 1) {
+      p.queue[0] = 0u;
+      p.queue[1] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 template <int D>
@@ -634,14 +750,17 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   }
   Params prm;
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.ntiles = ntiles;
+  prm.total = ntiles * a.Hk;
   prm.scale_log2 = a.scale * kLog2e;
   prm.o = (__nv_bfloat16*)a.o;
   prm.lse = a.lse;
   prm.err = a.err;
+  prm.queue = a.queue;
   cudaError_t e = cudaFuncSetAttribute(moda_fwd_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t grid = (int64_t)ntiles * a.Hk;
+  // one CTA per SM (each takes tiles from the queue until it is empty)
+  const int grid = min(prm.total, a.num_sms > 0 ? a.num_sms : 148);
   moda_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tkd, tvd, prm);
   return cudaGetLastError();
 }

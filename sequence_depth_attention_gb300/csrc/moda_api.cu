@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -14,6 +15,12 @@
 // Latched by kernels whose bounded waits give up; read and cleared by
 // moda_get_device_error. One copy per device (module-scope device variable).
 __device__ unsigned int g_moda_err = 0;
+
+// Tile queues of the persistent forward: {next tile, CTAs finished} per
+// slot. A launch takes the next slot in turn; its last CTA puts both back to
+// zero, so a slot is clean again when the launch has finished.
+constexpr int kQueueSlots = 64;
+__device__ unsigned int g_moda_queue[kQueueSlots][2] = {};
 
 namespace {
 
@@ -38,10 +45,12 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 struct DeviceEntry {
-  void* ctx = nullptr;            // context the cached address belongs to
+  void* ctx = nullptr;            // context the cached addresses belong to
   unsigned int* err = nullptr;    // device address of g_moda_err in it
+  unsigned int* queue = nullptr;  // device address of g_moda_queue in it
   int sms = 0;
 };
+std::atomic<unsigned int> g_queue_seq{0};
 DeviceEntry g_dev[kMaxDevices];
 
 // Current device, its error-word address and SM count; checks that it is
@@ -49,7 +58,8 @@ DeviceEntry g_dev[kMaxDevices];
 // is cached per device together with the context it was resolved in, and
 // resolved again when the current context differs (after cudaDeviceReset the
 // runtime creates a new primary context, and the module's variables move).
-moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out) {
+moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out,
+                         unsigned int** queue_out = nullptr) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0)
@@ -73,12 +83,18 @@ moda_status device_state(int* dev_out, unsigned int** err_out, int* sms_out) {
     if (e != cudaSuccess || !p)
       return fail(MODA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
     ent.err = (unsigned int*)p;
+    void* qp = nullptr;
+    e = cudaGetSymbolAddress(&qp, g_moda_queue);
+    if (e != cudaSuccess || !qp)
+      return fail(MODA_ERR_CUDA, "cudaGetSymbolAddress(tile queues): %s", cudaGetErrorString(e));
+    ent.queue = (unsigned int*)qp;
     ent.sms = sms;
     ent.ctx = moda::current_context();  // bound by now
   }
   *dev_out = dev;
   *err_out = ent.err;
   *sms_out = ent.sms;
+  if (queue_out) *queue_out = ent.queue + 2 * (g_queue_seq.fetch_add(1) % kQueueSlots);
   return MODA_OK;
 }
 
@@ -379,7 +395,7 @@ static moda_status prepare_fwd(const void* q, const void* k, const void* v, cons
   a.kd = L ? kd : nullptr; a.vd = L ? vd : nullptr;
   a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G;
   a.scale = scale; a.o = o; a.lse = lse;
-  return device_state(&a.device, &a.err, &a.num_sms);
+  return device_state(&a.device, &a.err, &a.num_sms, &a.queue);
 }
 
 moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd,

@@ -21,6 +21,7 @@ struct FwdArgs {
   void* o;         // [T, Hq, d] bf16
   float* lse;      // [T, Hq] fp32 or nullptr
   unsigned int* err;  // device error word of the current device
+  unsigned int* queue;  // {next tile, CTAs finished}, zero at launch, zero again at exit
   int num_sms;
   int device;
 };
