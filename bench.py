@@ -42,7 +42,8 @@ from sequence_depth_attention_gb300 import inputs as wl  # noqa: E402
 
 METRIC = "MoDA fwd TFLOP/s and % bf16 tensor peak at T=64K; overhead vs L=0"
 FWD_SOURCES = ["sequence_depth_attention_gb300/csrc/fwd_tc.cu",
-               "sequence_depth_attention_gb300/csrc/sm103.cuh"]
+               "sequence_depth_attention_gb300/csrc/sm103.cuh",
+               "sequence_depth_attention_gb300/csrc/softmax_block.cuh"]
 PACK_SOURCES = ["sequence_depth_attention_gb300/csrc/pack_depth.cu"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GB300 nominal dense bf16 tensor rate (no 2:4 sparsity), per GPU

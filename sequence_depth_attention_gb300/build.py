@@ -41,7 +41,8 @@ def _flags(extra=()):
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    headers = (glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+               glob.glob(os.path.join(INCLUDE, "*.h")))
     newest_header = max((os.path.getmtime(h) for h in headers), default=0)
     cc = nvcc()
 

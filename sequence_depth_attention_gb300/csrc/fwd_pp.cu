@@ -18,8 +18,11 @@
 // ahead of its P.V stream: S_X(j+1) once the softmax holds S_X(j) in
 // registers, P_X(j).V(j) once P_X(j) is stored (the S cursor runs at most
 // two blocks ahead of the P.V cursor).
-// A block may be used by A, B or both (the last sequence block, and the
-// depth blocks, which hold one tile's positions or both). Every K/V stage is
+// Depth blocks belong to one tile: as in the d = 128 kernel, each of its
+// softmax warps owns one 32-row word of the block, filled with the next packed
+// depth rows of the warp's own positions. A tile's depth blocks are its own
+// (A's first, then B's in the pair's schedule); the last sequence block may be
+// used by both tiles. Every K/V stage is
 // released by two arrivals per block, one per tile: the MMA commit of a tile
 // that used the block, or a plain arrive of one that did not, made only
 // after the block's full barrier, so an early arrival never completes the
@@ -32,6 +35,7 @@
 
 #include "moda_internal.h"
 #include "sm103.cuh"
+#include "softmax_block.cuh"
 #include "tensor_map.h"
 
 namespace moda {
@@ -106,13 +110,15 @@ struct PairGeom {
   int p0;       // first position of tile A (tile B starts at p0 + P)
   int npos[2];  // positions of A and B (0: B absent)
   int nb_seq[2];
+  int nd[2];    // depth blocks of A and B: ceil(min(npos, P/4) * L / 32)
   int n_depth, nb;
-  __device__ bool uses(int x, const PairSched& s, int L) const {
+  // the tile a depth block belongs to, and its index among that tile's
+  __device__ int depth_tile(int index) const { return index < nd[0] ? 0 : 1; }
+  __device__ int depth_index(int index) const { return index < nd[0] ? index : index - nd[0]; }
+  __device__ bool uses(int x, const PairSched& s) const {
     if (npos[x] == 0) return false;
     if (!s.depth) return s.index < nb_seq[x];
-    const int r0 = s.index * BN, r1 = r0 + BN;  // pair-relative depth rows of the block
-    const int lo = x * P * L, hi = lo + npos[x] * L;
-    return r0 < hi && r1 > lo;
+    return depth_tile(s.index) == x;
   }
 };
 
@@ -139,10 +145,12 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   g.npos[1] = g.p0 + g.P < p.T ? min(g.P, p.T - g.p0 - g.P) : 0;
   for (int x = 0; x < 2; ++x)
     g.nb_seq[x] = g.npos[x] ? (g.p0 + x * g.P + g.npos[x] - 1) / BN + 1 : 0;
-  const int nd = (g.npos[0] + g.npos[1]) * p.L;  // the pair's packed depth rows
-  g.n_depth = (nd + BN - 1) / BN;
+  const int PW = g.P >> 2;   // positions per softmax warp
+  const int RW = PW * p.L;   // packed depth rows per softmax warp
+  for (int x = 0; x < 2; ++x) g.nd[x] = (min(g.npos[x], PW) * p.L + 31) / 32;
+  g.n_depth = g.nd[0] + g.nd[1];
   g.nb = g.n_depth + max(g.nb_seq[0], g.nb_seq[1]);
-  const int depth_row0 = (hk * p.T + g.p0) * p.L;
+  const int depth_row0 = (hk * p.T + g.p0) * p.L;  // tile A's first packed depth row
 
   if (tid == 0) {
     bars->abort = 0;
@@ -208,9 +216,14 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, kTile);
           const uint32_t dst = sbase + s * kTile;
-          if (sch.depth)
-            tma_load_2d_hint(dst, dep_map, fb, 0, depth_row0 + sch.index * BN, pol_once);
-          else
+          if (sch.depth) {
+            // four 32-row words: rows [32w, 32w+32) of the stage hold softmax
+            // warp w's next 32 packed depth rows of the block's tile
+            const int x = g.depth_tile(sch.index);
+            const int r0 = depth_row0 + x * g.P * p.L + g.depth_index(sch.index) * 32;
+            for (int w = 0; w < 4; ++w)
+              tma_load_2d_hint(dst + w * 32 * 128, dep_map, fb, 0, r0 + w * RW, pol_once);
+          } else
             tma_load_3d(dst, seq_map, fb, 0, hk, sch.index * BN);
         }
         __syncwarp();
@@ -248,7 +261,7 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // the S cursor: block bs, used by this tile or only released by it
       auto advance_s = [&]() -> bool {
         ss.next(g.n_depth, g.nb);
-        const bool use = g.uses(x, ss, p.L);
+        const bool use = g.uses(x, ss);
         const int st = bs % kNS;
         const bool ok = (use && jS >= 1)
                             ? wait2(&bars->k_full[st], (bs / kNS) & 1, &bars->s_free[x], (jS - 1) & 1)
@@ -283,7 +296,7 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         while (ok && bs < g.nb && bs <= bp + 1) ok = advance_s();
         if (!ok) break;
         sp.next(g.n_depth, g.nb);
-        const bool use = g.uses(x, sp, p.L);
+        const bool use = g.uses(x, sp);
         const int st = bp % kNS;
         if (use) {
           if (!wait2(&bars->p_full[x], jP & 1, &bars->v_full[st], (bp / kNS) & 1)) break;
@@ -325,46 +338,107 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int h_row = hk * G + (row & (G - 1));
     const bool valid = lp < g.npos[tx];
     const int t_mask = min(t_row, p.T - 1);
-    const int d_lo = (tx * g.P + lp) * p.L;      // pair-relative depth rows of this row
-    const int d_hi = valid ? d_lo + p.L : d_lo;  // rows past T keep no depth column
+    const int wq = warp & 3;                       // this warp's word of a depth block
+    const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's rows
+    const int dw_n = valid ? p.L : 0;               // rows past T keep no depth column
     const float sl = p.scale_log2;
     const uint32_t colS = kColS + tx * 128, colO = kColO + tx * 64, colP = kColP + tx * 64;
+    const uint32_t zeros[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    bool p_zero = false;  // this warp's P columns outside its depth word hold zeros
     float m_ref = -INFINITY, l = 0.f;
     bool ok = g.npos[tx] > 0;
     int j = 0;  // blocks of this tile so far
+    // Rescale O and l to a new reference when a block's raw max mx (log2
+    // units) rose more than the threshold above it; false on a timeout.
+    auto rescale = [&](float mx) -> bool {
+      const bool need = mx > m_ref + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_ref;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+        if (j > 0) {
+          if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tmem_addr(tbase, lane_base, colO + c * 32);
+            tmem_ld32(ta, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(ta, r);
+          }
+          tmem_st_wait();
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      return true;
+    };
+    // stale-reference fast path checked by the block sum (every p is at most
+    // the sum, so a sum within 2^threshold proves the max did not rise past
+    // it); max-first slow path with a lazy rescale of O and l (as in the
+    // d = 128 kernel)
     PairSched sch;
     for (int b = 0; ok && b < g.nb; ++b) {
       sch.next(g.n_depth, g.nb);
-      if (!g.uses(tx, sch, p.L)) continue;
+      if (!g.uses(tx, sch)) continue;
       if (!warp_wait(smem_u32(&bars->s_full[tx]), j & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t x[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, colS + c * 32), x + c * 32);
-      tmem_ld_wait();
-      // S is in registers: the tile's S columns may take its next block
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free[tx]));
+      const uint32_t pcol = tmem_addr(tbase, lane_base, colP);
+      float sum = 0.f;
       if (sch.depth) {
-        // depth block: keep the row's own slots [lo, hi), one validity word per
-        // 32 columns (a bit test and a select per column)
-        const int lo = d_lo - sch.index * BN, hi = d_hi - sch.index * BN;
-        if (lo > 0 || hi < BN) {
+        // depth block: only this warp's word of 32 columns holds its rows'
+        // slots; the row keeps its own [lo, hi) (a bit test and a select)
+        uint32_t xs[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, colS + wq * 32), xs);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_free[tx]));
+        const int lo = dw_lo - g.depth_index(sch.index) * 32, hi = lo + dw_n;
+        const int a = min(max(lo, 0), 32), bb = min(max(hi, 0), 32);
+        const uint32_t word =
+            (bb >= 32 ? 0xffffffffu : (1u << bb) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
 #pragma unroll
-          for (int k = 0; k < BN / 32; ++k) {
-            const int a = min(max(lo - 32 * k, 0), 32), b = min(max(hi - 32 * k, 0), 32);
-            const uint32_t upto_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
-            const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
-            const uint32_t word = upto_b & ~below_a;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              x[32 * k + i] = (word & (1u << i)) ? x[32 * k + i] : 0xff800000u;  // -inf
-          }
+        for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
+        uint32_t pk[16];
+        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          sum = exp_block<32>(xs, pk, sl, m_ref);
+          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
         }
+        if (slow) {
+          if (!rescale(raw_max32(xs) * sl)) {
+            ok = false;
+            break;
+          }
+          sum = exp_block<32>(xs, pk, sl, m_ref);
+        }
+        l += sum;
+        // the tile's P columns hold P of its previous block until that P.V is done
+        if (j >= 1) {
+          if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(pcol + wq * 16, pk);
+        if (!p_zero) {
+          for (int k = 1; k < 4; ++k) tmem_st16(pcol + ((wq + k) & 3) * 16, zeros);
+        }
+        p_zero = true;
       } else {
+        uint32_t x[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, colS + c * 32), x + c * 32);
+        tmem_ld_wait();
+        // S is in registers: the tile's S columns may take its next block
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_free[tx]));
         // sequence block: the grouped causal mask keeps columns below hi
         const int k0 = sch.index * BN;
         if (k0 + BN - 1 > p0x) {
@@ -372,94 +446,32 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
           for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : 0xff800000u;  // -inf
         }
-      }
-      // row max of the raw scores (scaled after): three-input max tree
-      auto row_max = [&]() -> float {
-        float a1[43];
-#pragma unroll
-        for (int i = 0; i < 42; ++i)
-          a1[i] = max3f(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]),
-                        __uint_as_float(x[3 * i + 2]));
-        a1[42] = fmaxf(__uint_as_float(x[126]), __uint_as_float(x[127]));
-        float a2[15];
-#pragma unroll
-        for (int i = 0; i < 14; ++i) a2[i] = max3f(a1[3 * i], a1[3 * i + 1], a1[3 * i + 2]);
-        a2[14] = a1[42];
-        float a3[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) a3[i] = max3f(a2[3 * i], a2[3 * i + 1], a2[3 * i + 2]);
-        return fmaxf(max3f(a3[0], a3[1], a3[2]), fmaxf(a3[3], a3[4])) * sl;
-      };
-      uint32_t pk[BN / 2];
-      auto compute_p = [&](float m) -> float {
-        const float nbase = (m == -INFINITY) ? 0.f : -m;
-        const uint64_t sl2 = f2(sl, sl), nb2 = f2(nbase, nbase);
-        uint64_t acc[8];
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          float u, w;
-          f2_split(ffma2(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nb2), u, w);
-          const float e0 = ex2_approx(u), e1 = ex2_approx(w);
-          pk[c] = pack_bf16x2(e0, e1);
-          acc[c & 7] = c < 8 ? f2(e0, e1) : fadd2(acc[c & 7], f2(e0, e1));
+        uint32_t pk[BN / 2];
+        bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          sum = exp_block<BN>(x, pk, sl, m_ref);
+          slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
         }
-        acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-        acc[4] = fadd2(fadd2(acc[4], acc[5]), fadd2(acc[6], acc[7]));
-        acc[0] = fadd2(acc[0], acc[4]);
-        float u, w;
-        f2_split(acc[0], u, w);
-        return u + w;
-      };
-      // stale-reference fast path checked by the block sum (every p is at
-      // most the sum, so a sum within 2^threshold proves the max did not rise
-      // past it); max-first slow path with a lazy rescale of O and l (as in
-      // the d = 128 kernel)
-      float sum = 0.f;
-      bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
-      if (!slow) {
-        sum = compute_p(m_ref);
-        slow = __any_sync(0xffffffffu, !(sum <= kSumBound));
-      }
-      if (slow) {
-        const float mx = row_max();
-        const bool need = mx > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mx : m_ref;
-          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-          if (j > 0) {
-            if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              const uint32_t ta = tmem_addr(tbase, lane_base, colO + c * 32);
-              tmem_ld32(ta, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(ta, r);
-            }
-            tmem_st_wait();
+        if (slow) {
+          if (!rescale(raw_max128(x) * sl)) {
+            ok = false;
+            break;
           }
-          l *= alpha;
-          m_ref = m_new;
+          sum = exp_block<BN>(x, pk, sl, m_ref);
         }
-        sum = compute_p(m_ref);
-      }
-      l += sum;
-      // the tile's P columns hold P of its previous block until that P.V is done
-      if (j >= 1) {
-        if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
-          ok = false;
-          break;
+        l += sum;
+        // the tile's P columns hold P of its previous block until that P.V is done
+        if (j >= 1) {
+          if (!warp_wait(smem_u32(&bars->pv_done[tx]), (j - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-      }
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) tmem_st32(tmem_addr(tbase, lane_base, colP + c * 32), pk + c * 32);
+        for (int c = 0; c < BN / 64; ++c) tmem_st32(pcol + c * 32, pk + c * 32);
+        p_zero = false;
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[tx]));
@@ -524,7 +536,7 @@ cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
   if (a.L > 0) {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
     const uint64_t str[1] = {row};
-    const uint32_t box[2] = {64, BN};
+    const uint32_t box[2] = {64, 32};  // one softmax warp's word of a depth block
     if (encode_bf16_sw128(&tkd, a.kd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_bf16_sw128(&tvd, a.vd, 2, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   } else {
