@@ -27,8 +27,8 @@
 //     tensor core; o = O / l once at the end, lse = m ln2 + ln l.
 //
 // Persistent CTAs: the grid is one CTA per SM, and each CTA takes tiles from
-// a queue in global memory (KV-head-major, longest tiles first within a head,
-// as the hardware would dispatch one CTA per tile). The pipeline runs on
+// a queue in global memory, longest tiles first (KV-head-major once the K/V
+// of all heads overflow half of L2). The pipeline runs on
 // across tile boundaries: the next tile's Q and K/V blocks load while the
 // current one finishes, its first S = Q K^T products run during the current
 // tile's last block and epilogue, so a tile costs no launch, prologue or
@@ -113,7 +113,7 @@ struct alignas(8) Barriers {
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Params {
-  int T, Hq, Hk, L, lgG, ntiles, total;
+  int T, Hq, Hk, L, lgG, ntiles, total, head_major;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -127,13 +127,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// Geometry of one tile (queue entry o: KV-head-major, longest tiles first).
+// Geometry of one tile. Queue entry o: longest tiles first; KV-head-major
+// when the heads' K/V together overflow half of L2 (resident tiles then share
+// one or two heads' K/V), else heads interleaved (longest first over all
+// heads, which balances the last wave better when every head's K/V stays in
+// L2 anyway).
 struct Tile {
   int hk, p0, npos, t_last, PW, RW, n_depth, nb, depth_row0;
   __device__ void set(int o, const Params& p) {
     const int P = BM >> p.lgG;  // positions per tile
-    const int tile = p.ntiles - 1 - o % p.ntiles;
-    hk = o / p.ntiles;
+    const int tile = p.ntiles - 1 - (p.head_major ? o % p.ntiles : o / p.Hk);
+    hk = p.head_major ? o / p.ntiles : o % p.Hk;
     p0 = tile * P;
     npos = min(P, p.T - p0);
     t_last = p0 + npos - 1;
@@ -701,6 +705,8 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   Params prm;
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.ntiles = ntiles;
   prm.total = ntiles * a.Hk;
+  // K and V of every KV head, bf16: head-major order once they overflow half of L2
+  prm.head_major = (uint64_t)a.Hk * a.T * D * 2 * 2 > (64ull << 20) ? 1 : 0;
   prm.scale_log2 = a.scale * kLog2e;
   prm.o = (__nv_bfloat16*)a.o;
   prm.lse = a.lse;
