@@ -78,6 +78,7 @@ struct PpParams {
   int T, Hq, Hk, L, lgG, npairs;
   float scale_log2;
   __nv_bfloat16* o;
+  int o_v8;  // o is 32-byte aligned: rows go out in 32-byte stores
   float* lse;
   unsigned int* err;
 };
@@ -482,19 +483,23 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_after();
       const float inv = 1.f / l;
       __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
+      uint32_t r[D];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, colO + c * 32), r);
-        tmem_ld_wait();
-        uint32_t w[16];
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, colO + c * 32), r + c * 32);
+      tmem_ld_wait();
+      if (valid) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(r[16 * c + 2 * i]) * inv, __uint_as_float(r[16 * c + 2 * i + 1]) * inv);
+          if (p.o_v8) {
+            st_global_v8(orow + 16 * c, w);
+          } else {
+            reinterpret_cast<uint4*>(orow)[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(orow)[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
         }
       }
       if (valid && p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
@@ -547,6 +552,7 @@ cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.npairs = npairs;
   prm.scale_log2 = a.scale * kLog2e;
   prm.o = (__nv_bfloat16*)a.o;
+  prm.o_v8 = ((uintptr_t)a.o & 31u) == 0;
   prm.lse = a.lse;
   prm.err = a.err;
   cudaError_t e = cudaFuncSetAttribute(moda_fwd_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

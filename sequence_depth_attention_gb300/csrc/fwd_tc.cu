@@ -116,6 +116,7 @@ struct Params {
   int T, Hq, Hk, L, lgG, ntiles, total, head_major;
   float scale_log2;
   __nv_bfloat16* o;
+  int o_v8;  // o is 32-byte aligned: rows go out in 32-byte stores
   float* lse;
   unsigned int* err;
   unsigned int* queue;  // {next tile, CTAs finished}
@@ -635,14 +636,20 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const float inv = 1.f / l;
       __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
       if (valid) {
+        // 32-byte stores where o allows them (half the store instructions of
+        // 16-byte ones: each store of the warp touches 32 rows)
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[8 * c]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
-          reinterpret_cast<uint4*>(orow)[c] = v;
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            v[i] = pack_bf16x2(__uint_as_float(r[16 * c + 2 * i]) * inv, __uint_as_float(r[16 * c + 2 * i + 1]) * inv);
+          if (p.o_v8) {
+            st_global_v8(orow + 16 * c, v);
+          } else {
+            reinterpret_cast<uint4*>(orow)[2 * c] = make_uint4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<uint4*>(orow)[2 * c + 1] = make_uint4(v[4], v[5], v[6], v[7]);
+          }
         }
         if (p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
       }
@@ -709,6 +716,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   prm.head_major = (uint64_t)a.Hk * a.T * D * 2 * 2 > (64ull << 20) ? 1 : 0;
   prm.scale_log2 = a.scale * kLog2e;
   prm.o = (__nv_bfloat16*)a.o;
+  prm.o_v8 = ((uintptr_t)a.o & 31u) == 0;
   prm.lse = a.lse;
   prm.err = a.err;
   prm.queue = a.queue;

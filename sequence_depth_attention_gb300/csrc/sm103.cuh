@@ -261,6 +261,14 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef MODA_R8
 #undef MODA_W8
 
+// 32 bytes to global memory in one store (sm_100+ 256-bit access); p must be
+// 32-byte aligned (a misaligned address faults).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

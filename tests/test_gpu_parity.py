@@ -164,3 +164,25 @@ def test_lse_optional_and_status_clean():
     assert moda.moda_get_device_error() == 0
     o2, _ = moda.moda_fwd(x["q"], x["k"], x["v"], kd, vd, w.scale)
     assert torch.equal(o, o2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_16_byte_aligned_only(d):
+    """o at an address that is 16- but not 32-byte aligned (the ABI asks for
+    16): the rows go out in 16-byte stores, with the same values as from a
+    32-byte aligned o."""
+    w = Workload(f"o-align-d{d}", T=300, Hq=8, Hk=2, d=d, L=6, seed=31)
+    x = {n: t.cuda() for n, t in make_inputs(w).items()}
+    kd = moda.moda_pack_depth(x["kd"])
+    vd = moda.moda_pack_depth(x["vd"])
+    o_ref, l_ref = moda.moda_fwd(x["q"], x["k"], x["v"], kd, vd, w.scale)
+    n = w.T * w.Hq * w.d
+    buf = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+    base = buf.data_ptr()
+    off = next(e for e in range(0, 16) if (base + 2 * e) % 32 == 16)
+    o = buf[off:off + n].view(w.T, w.Hq, w.d)
+    assert o.data_ptr() % 32 == 16
+    moda.moda_fwd(x["q"], x["k"], x["v"], kd, vd, w.scale, o=o)
+    torch.cuda.synchronize()
+    assert moda.moda_get_device_error() == 0
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
