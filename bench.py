@@ -51,7 +51,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def workload_by_name(name):
-    for w in [*wl.ALL, wl.LONG_L0, *wl.TABLE2]:
+    for w in [*wl.ALL, wl.LONG_L0, wl.LONG_32K, *wl.TABLE2]:
         if w.name == name:
             return w
     raise SystemExit(f"unknown workload {name}; known: {[w.name for w in wl.ALL]}")

@@ -64,6 +64,10 @@ DEPTH_SWEEP = [Workload(f"depth-sweep-L{l}", T=16384, Hq=16, Hk=4, d=128, L=l)
                for l in (0, 8, 24, 48, 96)]
 LONG = Workload("long-64k", T=65536, Hq=16, Hk=4, d=128, L=48)
 LONG_L0 = LONG.with_L(0)
+# The long workload at half the length: small enough for multi-counter ncu
+# captures (about 3.6 GB on the device); every stream of the forward (q, o,
+# the depth rows, each KV head's K/V read once) scales with T.
+LONG_32K = Workload("long-32k", T=32768, Hq=16, Hk=4, d=128, L=48)
 
 ALL = [TINY, LAYER_700M, *GQA_SWEEP, *DEPTH_SWEEP, LONG]
 
