@@ -5,16 +5,20 @@
     python bench.py --impl reference ...        # the fp64 CPU oracle arm
 
 One step = the whole hot path over one batch of synthetic input resident in
-HBM: moda_pack_depth(kd), moda_pack_depth(vd), moda_fwd(...). The headline
-workload is the long-context layer (T=65536, Hq=16, Hk=4, d=128, L=48).
+HBM: moda_fwd_layer_major(...) on the depth K/V as the layers wrote them
+([L,T,Hk,d]); the depth relayout (the chunk-aware grouping) happens inside the
+forward's copies. The packed path (moda_pack_depth(kd), moda_pack_depth(vd),
+moda_fwd) is timed beside it. The headline workload is the long-context layer
+(T=65536, Hq=16, Hk=4, d=128, L=48).
 Throughput counts 4*d*Hq*(T(T+1)/2 + T*L) FLOPs per step (causal and valid
 depth work only). Under torchrun each rank runs an independent replica on its
 own GPU (weak scaling); value = all ranks' FLOPs / the slowest rank's time.
 
 Also reported on the same JSON line:
-  fwd             moda_fwd alone (CUDA events on its stream), % of bf16 peak
+  fwd             the step's forward (CUDA events on its stream), % of bf16 peak
+  packed_path     pack kd + pack vd + moda_fwd on the packed streams
   overhead_vs_L0  t_fwd(L) / t_fwd(L=0) - 1 for the same T, Hq, Hk, d
-  roofline        the dominant kernel (moda_fwd) against the measured peak
+  roofline        the dominant kernel (the forward) against the measured peak
   e2e             same metric with inputs copied from pinned host memory and
                   o, lse copied back inside the timed region
   cpu_baseline    the fp64 oracle on the host cores, on a bounded row sample
@@ -265,9 +269,10 @@ def time_calls(fn, stream, n, flush=None):
 def config_sweep(moda, dev, stream, peaks, steps, warmup):
     """moda_fwd on every workload other than the headline one: time, TFLOP/s,
     fraction of peak, the L = 0 forward of the same shape and the overhead of
-    the depth slots in both conventions, and the CUDA-core depth variant
-    beside the fused one. L2 is flushed (512 MB written) before every timed
-    call, so no workload runs out of a warm L2."""
+    the depth slots in both conventions, the CUDA-core depth variant beside
+    the fused one, and the layer-major forward and the two depth packs (the
+    two ways to the same result). L2 is flushed (512 MB written) before every
+    timed call, so no workload runs out of a warm L2."""
     peak = float(peaks["bf16_tflops"])
     flush = torch.empty(128 << 20, dtype=torch.float32, device=dev)
     out = {}
@@ -276,6 +281,7 @@ def config_sweep(moda, dev, stream, peaks, steps, warmup):
         q, k, v = x["q"], x["k"], x["v"]
         kd = moda.moda_pack_depth(x["kd"], stream=stream) if w.L else None
         vd = moda.moda_pack_depth(x["vd"], stream=stream) if w.L else None
+        kd_lm, vd_lm = x["kd"], x["vd"]
         del x
         o = torch.empty_like(q)
         lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device=dev)
@@ -299,15 +305,28 @@ def config_sweep(moda, dev, stream, peaks, steps, warmup):
             for _ in range(2):
                 fwd(cc=True)
             ms_cc = time_calls(lambda: fwd(cc=True), stream, max(3, steps // 2), flush)
+            def fwd_lm():
+                moda.moda_fwd_layer_major(q, k, v, kd_lm, vd_lm, w.scale, o=o, lse=lse, stream=stream)
+
+            def packs():
+                moda.moda_pack_depth(kd_lm, kd, stream=stream)
+                moda.moda_pack_depth(vd_lm, vd, stream=stream)
+
+            for _ in range(warmup):
+                fwd_lm()
+            ms_lm = time_calls(fwd_lm, stream, steps, flush)
+            ms_pack = time_calls(packs, stream, max(3, steps // 2), flush)
             rec.update({"L0_ms": ms0, "overhead_vs_L0": ms / ms0 - 1.0,
                         "extra_time_pages_convention": 1.0 - ms0 / ms,
                         "cuda_core_depth_ms": ms_cc,
-                        "faster_depth": "tensor cores" if ms <= ms_cc else "cuda cores"})
+                        "faster_depth": "tensor cores" if ms <= ms_cc else "cuda cores",
+                        "layer_major_ms": ms_lm, "layer_major_tflops": F / (ms_lm * 1e-3) / 1e12,
+                        "pack_kd_vd_ms": ms_pack})
         st = moda.moda_get_device_error(stream)
         if st != 0:
             raise SystemExit(f"device error in the sweep ({w.name}): {moda.moda_status_string(st)}")
         out[w.name] = rec
-        del q, k, v, kd, vd, o, lse
+        del q, k, v, kd, vd, kd_lm, vd_lm, o, lse
     del flush
     torch.cuda.empty_cache()
     return out
@@ -376,22 +395,34 @@ def main(argv=None):
               for _ in range(K)]
     pack_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
+    pfwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
 
+    # The step: the forward on the depth K/V as the layers wrote them
+    # ([L,T,Hk,d]); its copies gather each tile's depth rows (the depth
+    # relayout happens inside the forward, no separate pass).
     def step(i=None):
         if i is not None:
-            pack_ev[i][0].record(stream)
-        if w.L:
-            moda.moda_pack_depth(kd_raw, kd, stream=stream)
-            moda.moda_pack_depth(vd_raw, vd, stream=stream)
-        if i is not None:
-            pack_ev[i][1].record(stream)
             fwd_ev[i][0].record(stream)
-        moda.moda_fwd(q, k, v, kd if w.L else None, vd if w.L else None, w.scale, o=o, lse=lse,
-                      stream=stream)
+        moda.moda_fwd_layer_major(q, k, v, kd_raw if w.L else None, vd_raw if w.L else None,
+                                  w.scale, o=o, lse=lse, stream=stream)
         if i is not None:
             fwd_ev[i][1].record(stream)
 
-    launches_per_step = (2 if w.L else 0) + 1
+    # The packed path beside it: two moda_pack_depth passes, then moda_fwd on
+    # the packed streams (timed after the headline, not part of its step).
+    def packed_step(i):
+        pack_ev[i][0].record(stream)
+        if w.L:
+            moda.moda_pack_depth(kd_raw, kd, stream=stream)
+            moda.moda_pack_depth(vd_raw, vd, stream=stream)
+        pack_ev[i][1].record(stream)
+        pfwd_ev[i][0].record(stream)
+        moda.moda_fwd(q, k, v, kd if w.L else None, vd if w.L else None, w.scale, o=o, lse=lse,
+                      stream=stream)
+        pfwd_ev[i][1].record(stream)
+
+    launches_per_step = 1
 
     def barrier():
         if dist is not None:
@@ -417,10 +448,26 @@ def main(argv=None):
     clk = clocks.stop()
     ms_step = max_over_ranks(start.elapsed_time(end) / K, dist, dev)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
-    pack_ms = statistics.mean(a.elapsed_time(b) for a, b in pack_ev)
     st = moda.moda_get_device_error(stream)
     if st != 0:
         raise SystemExit(f"device error in timed region: {moda.moda_status_string(st)}")
+
+    # the packed path: pack kd and vd, then moda_fwd on the packed streams
+    for i in range(min(W, K)):
+        packed_step(i)
+    torch.cuda.synchronize(dev)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for i in range(K):
+        packed_step(i)
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    packed_step_ms = p0.elapsed_time(p1) / K
+    pack_ms = statistics.mean(a.elapsed_time(b) for a, b in pack_ev)
+    pfwd_ms = statistics.mean(a.elapsed_time(b) for a, b in pfwd_ev)
+    st = moda.moda_get_device_error(stream)
+    if st != 0:
+        raise SystemExit(f"device error in the packed path: {moda.moda_status_string(st)}")
 
     # plain causal GQA (L = 0) with the same kernel, same T/Hq/Hk/d
     w0 = w.with_L(0)
@@ -443,7 +490,8 @@ def main(argv=None):
     fwd0_tflops = w0.flops() / (fwd0_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     pack_bytes = 2 * 2 * (w.L * w.T * w.Hk * w.d * 2)  # read + write, kd and vd
-    traffic = recorded_traffic("moda_fwd", w.name, FWD_SOURCES)
+    traffic = recorded_traffic("moda_fwd_layer_major", w.name, FWD_SOURCES)
+    pfwd_tflops = F / (pfwd_ms * 1e-3) / 1e12
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -459,15 +507,21 @@ def main(argv=None):
         "fwd_L0": {"ms": fwd0_ms, "tflops": fwd0_tflops, "pct_peak_burst": 100 * fwd0_tflops / peak},
         "overhead_vs_L0": fwd_ms / fwd0_ms - 1.0,
         "extra_time_pages_convention": 1.0 - fwd0_ms / fwd_ms,
-        "pack": {"ms_for_kd_and_vd": pack_ms,
-                 "gbs": (pack_bytes / (pack_ms * 1e-3) / 1e9) if w.L and pack_ms > 0 else None,
-                 "pct_hbm": (100 * pack_bytes / (pack_ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
-                 if w.L and pack_ms > 0 else None},
+        "packed_path": {
+            "step_ms": packed_step_ms, "tflops": F / (packed_step_ms * 1e-3) / 1e12,
+            "fwd_ms": pfwd_ms, "fwd_tflops": pfwd_tflops,
+            "fwd_pct_peak_burst": 100 * pfwd_tflops / peak,
+            "pack": {"ms_for_kd_and_vd": pack_ms,
+                     "gbs": (pack_bytes / (pack_ms * 1e-3) / 1e9) if w.L and pack_ms > 0 else None,
+                     "pct_hbm": (100 * pack_bytes / (pack_ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
+                     if w.L and pack_ms > 0 else None},
+            "note": "moda_pack_depth(kd) + moda_pack_depth(vd) + moda_fwd on the packed "
+                    "[Hk,T,L,d] streams, the same result"},
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": fwd_tflops / peak, "traffic": traffic,
                      "peak_source": f"{peaks_src} bf16 dense burst (MEASURED_PEAKS.json)"
                      if peaks_src == "measured" else "fallback 1.9 PFLOP/s bf16",
-                     "kernel": "moda_fwd"},
+                     "kernel": "moda_fwd_layer_major (moda_fwd_tc_kernel<128>)"},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
@@ -482,7 +536,7 @@ def main(argv=None):
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         # Double-buffered device inputs: the copy engines move step i+1's
         # inputs (every byte of them, from pinned host memory) while step i
-        # packs and runs on the compute stream; the host link is the bound.
+        # runs on the compute stream; the host link is the bound.
         copy = torch.cuda.Stream(device=dev)
         sets = [(q, k, v, kd_raw, vd_raw)]
         sets.append(tuple(torch.empty_like(t) for t in sets[0]))
@@ -506,7 +560,7 @@ def main(argv=None):
 
         def e2e_step(n):
             """Step i of n: waits for its inputs, starts step i+1's copy (unless
-            it is the last), then packs, runs and reads back."""
+            it is the last), then runs the forward and reads back."""
             i = n_issued[0]
             n_issued[0] += 1
             if i == 0:
@@ -515,11 +569,8 @@ def main(argv=None):
             if i + 1 < n:
                 issue_copy(i + 1)  # overlaps this step's compute
             dq, dk, dv, dkr, dvr = sets[i % 2]
-            if w.L:
-                moda.moda_pack_depth(dkr, kd, stream=stream)
-                moda.moda_pack_depth(dvr, vd, stream=stream)
-            moda.moda_fwd(dq, dk, dv, kd if w.L else None, vd if w.L else None, w.scale, o=o,
-                          lse=lse, stream=stream)
+            moda.moda_fwd_layer_major(dq, dk, dv, dkr if w.L else None, dvr if w.L else None,
+                                      w.scale, o=o, lse=lse, stream=stream)
             consumed[i % 2].record(stream)
             with torch.cuda.stream(stream):
                 ho.copy_(o, non_blocking=True)
@@ -545,7 +596,7 @@ def main(argv=None):
                        "d2h_bytes_per_step": d2h,
                        "transfer": "every step's q, k, v, kd, vd copied from pinned host memory by "
                                    "the copy engines into one of two device input sets, overlapping "
-                                   "the previous step's pack + forward; o, lse copied back each step; "
+                                   "the previous step's forward; o, lse copied back each step; "
                                    "the timed region runs from the first step's copy to the last "
                                    "step's read-back"}
         host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}

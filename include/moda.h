@@ -234,6 +234,25 @@ MODA_API moda_status moda_fwd(const void* q, const void* k, const void* v,
                      moda_stream_t stream);
 
 /*
+ * moda_fwd_layer_major -- moda_fwd on the depth K/V in the order the layers
+ * write them, with no relayout pass: the chunk-aware grouping of Sec. 3.2
+ * (Fig. 4: a query tile's depth rows side by side) happens inside the
+ * forward's tensor-memory-accelerator copies, which gather each depth block
+ * from the layer-major tensors straight into shared memory. Same result as
+ * moda_pack_depth(kd) + moda_pack_depth(vd) + moda_fwd, to rounding order.
+ *
+ *   kd, vd  [L, T, Hk, d] bf16: slot l of position t for KV head hk at
+ *           [l][t][hk][:] (the layout moda_pack_depth takes as its source);
+ *           may be NULL when L == 0
+ *   every other argument, the arithmetic, the supported shapes and the
+ *   errors as moda_fwd.
+ */
+MODA_API moda_status moda_fwd_layer_major(const void* q, const void* k, const void* v,
+                                          const void* kd, const void* vd, int T, int Hq,
+                                          int Hk, int d, int L, float scale, void* o,
+                                          float* lse, moda_stream_t stream);
+
+/*
  * moda_fwd_depth_cc -- the same result as moda_fwd, with the depth slots on
  * CUDA cores instead of tensor cores: the sequence part runs as moda_fwd with
  * L = 0, then one warp per (KV head, position) reads that position's L slots

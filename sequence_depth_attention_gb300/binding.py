@@ -26,7 +26,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
 # every symbol include/moda.h declares
 EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_depth_write_at", "moda_depth_mass",
            "moda_depth_mass_workspace_bytes", "moda_depth_cache_admit", "moda_kv_proj_write",
-           "moda_fwd", "moda_fwd_depth_cc", "moda_decode",
+           "moda_fwd", "moda_fwd_layer_major", "moda_fwd_depth_cc", "moda_decode",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
@@ -79,6 +79,8 @@ def load():
         lib.moda_fwd_depth_cc.restype = i
         lib.moda_fwd_depth_cc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd.restype = i
+        lib.moda_fwd_layer_major.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
+        lib.moda_fwd_layer_major.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
         lib.moda_bwd.restype = i
         lib.moda_bwd_noalloc.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 6
@@ -278,6 +280,39 @@ def moda_fwd(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L, float(scale), _ptr(o),
             _ptr(lse), _stream(stream))
     _check(st, name)
+    return o, lse
+
+
+def moda_fwd_layer_major(q, k, v, kd, vd, scale: float, o=None, lse=None, stream=None,
+                         want_lse: bool = True):
+    """MoDA forward on layer-major depth K/V: kd/vd [L,T,Hk,d] as the layers
+    wrote them (or None when L == 0); the forward gathers each depth block
+    itself, no relayout pass. Returns (o[T,Hq,d] bf16, lse[T,Hq] fp32 or None)."""
+    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    T, Hq, d = q.shape
+    Hk = k.shape[1]
+    if tuple(k.shape) != (T, Hk, d) or tuple(v.shape) != (T, Hk, d):
+        raise ValueError("k and v must be [T,Hk,d] matching q[T,Hq,d]")
+    if kd is None or kd.numel() == 0:
+        L = 0 if kd is None else kd.shape[0]
+        if L != 0:
+            raise ValueError("empty kd with L > 0")
+        kd = vd = None
+    else:
+        _need(kd, "kd"), _need(vd, "vd")
+        L = kd.shape[0]
+        if tuple(kd.shape) != (L, T, Hk, d) or tuple(vd.shape) != (L, T, Hk, d):
+            raise ValueError(f"kd/vd must be layer-major [L,T,Hk,d] = {(L, T, Hk, d)}")
+    if o is None:
+        o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=q.device)
+    _need(o, "o")
+    if want_lse and lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    st = load().moda_fwd_layer_major(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L,
+                                     float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check(st, "moda_fwd_layer_major")
     return o, lse
 
 

@@ -76,6 +76,7 @@ static_assert(sizeof(PpBars) <= 512, "barrier block");
 
 struct PpParams {
   int T, Hq, Hk, L, lgG, npairs;
+  int depth_lm;  // depth K/V layer-major [L, T, Hk, d] (else packed [Hk, T, L, d])
   float scale_log2;
   __nv_bfloat16* o;
   int o_v8;  // o is 32-byte aligned: rows go out in 32-byte stores
@@ -148,7 +149,10 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     g.nb_seq[x] = g.npos[x] ? (g.p0 + x * g.P + g.npos[x] - 1) / BN + 1 : 0;
   const int PW = g.P >> 2;   // positions per softmax warp
   const int RW = PW * p.L;   // packed depth rows per softmax warp
-  for (int x = 0; x < 2; ++x) g.nd[x] = (min(g.npos[x], PW) * p.L + 31) / 32;
+  // a word holds 32 rows: 32 consecutive packed rows, or (layer-major) PW
+  // positions x 32/PW slots
+  for (int x = 0; x < 2; ++x)
+    g.nd[x] = g.npos[x] ? ((p.depth_lm ? PW : min(g.npos[x], PW)) * p.L + 31) / 32 : 0;
   g.n_depth = g.nd[0] + g.nd[1];
   g.nb = g.n_depth + max(g.nb_seq[0], g.nb_seq[1]);
   const int depth_row0 = (hk * p.T + g.p0) * p.L;  // tile A's first packed depth row
@@ -221,9 +225,18 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // four 32-row words: rows [32w, 32w+32) of the stage hold softmax
             // warp w's next 32 packed depth rows of the block's tile
             const int x = g.depth_tile(sch.index);
-            const int r0 = depth_row0 + x * g.P * p.L + g.depth_index(sch.index) * 32;
-            for (int w = 0; w < 4; ++w)
-              tma_load_2d_hint(dst + w * 32 * 128, dep_map, fb, 0, r0 + w * RW, pol_once);
+            if (p.depth_lm) {
+              // layer-major: the copy gathers slots [SP*i, SP*i + SP) of warp
+              // w's PW positions, row l_local*PW + t_local (SP = 32/PW)
+              const int SP = 32 / PW;
+              for (int w = 0; w < 4; ++w)
+                tma_load_4d_hint(dst + w * 32 * 128, dep_map, fb, 0, hk, g.p0 + x * g.P + w * PW,
+                                 g.depth_index(sch.index) * SP, pol_once);
+            } else {
+              const int r0 = depth_row0 + x * g.P * p.L + g.depth_index(sch.index) * 32;
+              for (int w = 0; w < 4; ++w)
+                tma_load_2d_hint(dst + w * 32 * 128, dep_map, fb, 0, r0 + w * RW, pol_once);
+            }
           } else
             tma_load_3d(dst, seq_map, fb, 0, hk, sch.index * BN);
         }
@@ -342,6 +355,11 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int wq = warp & 3;                       // this warp's word of a depth block
     const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's rows
     const int dw_n = valid ? p.L : 0;               // rows past T keep no depth column
+    // layer-major words: column c holds position c % PW of the warp's
+    // positions, slot index*(32/PW) + c / PW; this row's columns are
+    // c = its position + i*PW
+    const int lpw = (row & 31) >> p.lgG;
+    const uint32_t lm_pat = PW >= 32 ? 1u << lpw : (0xffffffffu / ((1u << PW) - 1u)) << lpw;
     const float sl = p.scale_log2;
     const uint32_t colS = kColS + tx * 128, colO = kColO + tx * 64, colP = kColP + tx * 64;
     const uint32_t zeros[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
@@ -399,10 +417,16 @@ moda_fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->s_free[tx]));
-        const int lo = dw_lo - g.depth_index(sch.index) * 32, hi = lo + dw_n;
-        const int a = min(max(lo, 0), 32), bb = min(max(hi, 0), 32);
-        const uint32_t word =
-            (bb >= 32 ? 0xffffffffu : (1u << bb) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+        uint32_t word;
+        if (p.depth_lm) {
+          const int SP = 32 / PW;
+          const int nbits = min(SP, p.L - g.depth_index(sch.index) * SP) * PW;  // slots < L
+          word = valid ? lm_pat & (nbits >= 32 ? 0xffffffffu : (1u << nbits) - 1u) : 0u;
+        } else {
+          const int lo = dw_lo - g.depth_index(sch.index) * 32, hi = lo + dw_n;
+          const int a = min(max(lo, 0), 32), bb = min(max(hi, 0), 32);
+          word = (bb >= 32 ? 0xffffffffu : (1u << bb) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
         uint32_t pk[16];
@@ -538,7 +562,15 @@ cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
     if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  if (a.L > 0) {
+  if (a.L > 0 && a.layer_major) {
+    // [L, T, Hk, d]: a box is one softmax warp's word, PW positions x 32/PW slots
+    const uint32_t PW = (uint32_t)(P >> 2);
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T, (uint64_t)a.L};
+    const uint64_t str[3] = {row, row * a.Hk, row * a.Hk * a.T};
+    const uint32_t box[4] = {64, 1, PW, 32 / PW};
+    if (encode_bf16_sw128(&tkd, a.kd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  } else if (a.L > 0) {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
     const uint64_t str[1] = {row};
     const uint32_t box[2] = {64, 32};  // one softmax warp's word of a depth block
@@ -550,6 +582,7 @@ cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
   }
   PpParams prm;
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.npairs = npairs;
+  prm.depth_lm = a.layer_major;
   prm.scale_log2 = a.scale * kLog2e;
   prm.o = (__nv_bfloat16*)a.o;
   prm.o_v8 = ((uintptr_t)a.o & 31u) == 0;

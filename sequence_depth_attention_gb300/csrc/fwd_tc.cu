@@ -114,6 +114,7 @@ static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Params {
   int T, Hq, Hk, L, lgG, ntiles, total, head_major;
+  int depth_lm;  // depth K/V layer-major [L, T, Hk, d] (else packed [Hk, T, L, d])
   float scale_log2;
   __nv_bfloat16* o;
   int o_v8;  // o is 32-byte aligned: rows go out in 32-byte stores
@@ -144,7 +145,9 @@ struct Tile {
     t_last = p0 + npos - 1;
     PW = P >> 2;                     // positions per softmax warp
     RW = PW * p.L;                   // packed depth rows per softmax warp
-    n_depth = (min(npos, PW) * p.L + 31) / 32;
+    // a word holds 32 rows: 32 consecutive packed rows, or (layer-major) PW
+    // positions x 32/PW slots
+    n_depth = ((p.depth_lm ? PW : min(npos, PW)) * p.L + 31) / 32;
     nb = n_depth + t_last / BN + 1;
     depth_row0 = (hk * p.T + p0) * p.L;
   }
@@ -308,11 +311,22 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           if (sch.depth) {
             // four 32-row words: rows [32w, 32w+32) of the stage hold warp w's
             // packed depth rows 32*index .. +32 (128-byte swizzle atoms are 8
-            // rows, so a word starts on an atom boundary)
-            for (int w = 0; w < 4; ++w)
-              for (int c = 0; c < C::kBoxes; ++c)
-                tma_load_2d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64,
-                                 tl.depth_row0 + w * tl.RW + sch.index * 32, pol_once);
+            // rows, so a word starts on an atom boundary). Layer-major depth:
+            // the copy gathers the same word shape itself, slots
+            // [SP*index, SP*index + SP) of warp w's PW positions, row
+            // l_local*PW + t_local (SP = 32/PW)
+            if (p.depth_lm) {
+              const int SP = 32 / tl.PW;
+              for (int w = 0; w < 4; ++w)
+                for (int c = 0; c < C::kBoxes; ++c)
+                  tma_load_4d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64, tl.hk,
+                                   tl.p0 + w * tl.PW, sch.index * SP, pol_once);
+            } else {
+              for (int w = 0; w < 4; ++w)
+                for (int c = 0; c < C::kBoxes; ++c)
+                  tma_load_2d_hint(dst + c * C::kBoxBytes + w * 32 * 128, dep_map, fb, c * 64,
+                                   tl.depth_row0 + w * tl.RW + sch.index * 32, pol_once);
+            }
           } else {
             for (int c = 0; c < C::kBoxes; ++c)
               tma_load_3d(dst + c * C::kBoxBytes, seq_map, fb, c * 64, tl.hk, sch.index * BN);
@@ -483,6 +497,11 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const int t_mask = min(t_row, p.T - 1);
       const int dw_lo = ((row & 31) >> p.lgG) * p.L;  // the row's slots among its warp's RW rows
       const int dw_n = valid ? p.L : 0;             // rows past T keep no depth column
+      // layer-major words: column c holds position c % PW of the warp's
+      // positions, slot index*(32/PW) + c / PW; this row's columns are
+      // c = its position + i*PW
+      const int lpw = (row & 31) >> p.lgG;
+      const uint32_t lm_pat = tl.PW >= 32 ? 1u << lpw : (0xffffffffu / ((1u << tl.PW) - 1u)) << lpw;
       float m_ref = -INFINITY, l = 0.f;
       // Rescale O and l to a new reference when a block's raw max mx (log2
       // units) rose more than the threshold above it; false on a timeout.
@@ -538,10 +557,16 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(smem_u32(&bars->s_free[sb]));
-          const int lo = dw_lo - sch.index * 32, hi = lo + dw_n;
-          const int a = min(max(lo, 0), 32), b = min(max(hi, 0), 32);
-          const uint32_t word =
-              (b >= 32 ? 0xffffffffu : (1u << b) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+          uint32_t word;
+          if (p.depth_lm) {
+            const int SP = 32 / tl.PW;
+            const int nbits = min(SP, p.L - sch.index * SP) * tl.PW;  // columns of slots < L
+            word = valid ? lm_pat & (nbits >= 32 ? 0xffffffffu : (1u << nbits) - 1u) : 0u;
+          } else {
+            const int lo = dw_lo - sch.index * 32, hi = lo + dw_n;
+            const int a = min(max(lo, 0), 32), b = min(max(hi, 0), 32);
+            word = (b >= 32 ? 0xffffffffu : (1u << b) - 1u) & ~(a >= 32 ? 0xffffffffu : (1u << a) - 1u);
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) xs[i] = (word & (1u << i)) ? xs[i] : 0xff800000u;  // -inf
           uint32_t pk[16];
@@ -699,7 +724,15 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
     if (encode_bf16_sw128(&tk, a.k, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_bf16_sw128(&tv, a.v, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  if (a.L > 0) {
+  if (a.L > 0 && a.layer_major) {
+    // [L, T, Hk, d]: a box is one softmax warp's word, PW positions x 32/PW slots
+    const uint32_t PW = (uint32_t)(P >> 2);
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T, (uint64_t)a.L};
+    const uint64_t str[3] = {row, row * a.Hk, row * a.Hk * a.T};
+    const uint32_t box[4] = {64, 1, PW, 32 / PW};
+    if (encode_bf16_sw128(&tkd, a.kd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  } else if (a.L > 0) {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
     const uint64_t str[1] = {row};
     const uint32_t box[2] = {64, 32};  // one softmax warp's word of a depth block
@@ -711,6 +744,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   }
   Params prm;
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.ntiles = ntiles;
+  prm.depth_lm = a.layer_major;
   prm.total = ntiles * a.Hk;
   // K and V of every KV head, bf16: head-major order once they overflow half of L2
   prm.head_major = (uint64_t)a.Hk * a.T * D * 2 * 2 > (64ull << 20) ? 1 : 0;

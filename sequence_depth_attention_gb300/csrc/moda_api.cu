@@ -356,7 +356,7 @@ moda_status moda_kv_proj_write(const void* x, const void* wk, const void* wv, in
 // Validation shared by the forward entry points; fills *out on success.
 static moda_status prepare_fwd(const void* q, const void* k, const void* v, const void* kd,
                                const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
-                               void* o, float* lse, moda::FwdArgs* out) {
+                               void* o, float* lse, moda::FwdArgs* out, int layer_major = 0) {
   if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL q, k, v or o");
   if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
   if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
@@ -395,6 +395,7 @@ static moda_status prepare_fwd(const void* q, const void* k, const void* v, cons
   a.kd = L ? kd : nullptr; a.vd = L ? vd : nullptr;
   a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G;
   a.scale = scale; a.o = o; a.lse = lse;
+  a.layer_major = layer_major;
   return device_state(&a.device, &a.err, &a.num_sms, &a.queue);
 }
 
@@ -406,6 +407,18 @@ moda_status moda_fwd(const void* q, const void* k, const void* v, const void* kd
   if (st != MODA_OK) return st;
   cudaError_t e = moda::launch_fwd_tc(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_fwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+moda_status moda_fwd_layer_major(const void* q, const void* k, const void* v, const void* kd,
+                                 const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
+                                 void* o, float* lse, moda_stream_t stream) {
+  moda::FwdArgs a;
+  moda_status st = prepare_fwd(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, &a, 1);
+  if (st != MODA_OK) return st;
+  cudaError_t e = moda::launch_fwd_tc(a, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(MODA_ERR_CUDA, "moda_fwd_layer_major launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

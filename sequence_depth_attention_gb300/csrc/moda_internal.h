@@ -14,9 +14,10 @@ struct FwdArgs {
   const void* q;   // [T, Hq, d]
   const void* k;   // [T, Hk, d]
   const void* v;   // [T, Hk, d]
-  const void* kd;  // [Hk, T, L, d] packed, or nullptr when L == 0
-  const void* vd;  // [Hk, T, L, d] packed, or nullptr when L == 0
+  const void* kd;  // [Hk, T, L, d] packed (or [L, T, Hk, d] when layer_major), nullptr when L == 0
+  const void* vd;  // same layout as kd
   int T, Hq, Hk, d, L, G;
+  int layer_major;  // kd/vd as the layers wrote them: [L, T, Hk, d]
   float scale;
   void* o;         // [T, Hq, d] bf16
   float* lse;      // [T, Hq] fp32 or nullptr

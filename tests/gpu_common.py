@@ -25,10 +25,19 @@ def ensure_built():
     moda.load()
 
 
-def run_cuda(x, scale, device="cuda", depth_on_cuda_cores=False):
-    """x: dict of bf16 tensors (kd/vd in [L,T,Hk,d]). Returns o, lse on CPU."""
+def run_cuda(x, scale, device="cuda", depth_on_cuda_cores=False, layer_major=False):
+    """x: dict of bf16 tensors (kd/vd in [L,T,Hk,d]). Returns o, lse on CPU.
+    layer_major=True hands kd/vd to moda_fwd_layer_major as they are, else
+    they are packed first and go to moda_fwd."""
     q, k, v = (x[n].to(device) for n in ("q", "k", "v"))
     L = x["kd"].shape[0]
+    if layer_major:
+        kd = x["kd"].to(device).contiguous() if L else None
+        vd = x["vd"].to(device).contiguous() if L else None
+        o, lse = moda.moda_fwd_layer_major(q, k, v, kd, vd, scale)
+        torch.cuda.synchronize()
+        assert moda.moda_get_device_error() == 0
+        return o.float().cpu().numpy(), lse.cpu().numpy()
     if L:
         kd = moda.moda_pack_depth(x["kd"].to(device))
         vd = moda.moda_pack_depth(x["vd"].to(device))
@@ -60,13 +69,13 @@ def compare(x, scale, o, lse, ts=None, hs=None):
 
 
 def check_workload(w: Workload, sampled=False, device_inputs=False, q_mul=1.0,
-                   depth_on_cuda_cores=False, prep=None):
+                   depth_on_cuda_cores=False, prep=None, layer_major=False):
     x = make_inputs(w, device="cuda" if device_inputs else "cpu")
     if q_mul != 1.0:
         x["q"] = (x["q"].float() * q_mul).to(torch.bfloat16)
     if prep is not None:  # reshape the inputs' statistics (same tensors go to the oracle)
         x = prep(x)
-    o, lse = run_cuda(x, w.scale, depth_on_cuda_cores=depth_on_cuda_cores)
+    o, lse = run_cuda(x, w.scale, depth_on_cuda_cores=depth_on_cuda_cores, layer_major=layer_major)
     if device_inputs:
         x = {n: t.cpu() for n, t in x.items()}
     assert np.isfinite(o).all() and np.isfinite(lse).all()

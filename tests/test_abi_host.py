@@ -85,6 +85,21 @@ def test_fwd_rejects(lib, kw, code):
     assert lib.moda_last_error_detail().decode() != ""
 
 
+def fwd_lm(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.125, o=O, lse=LSE):
+    return lib.moda_fwd_layer_major(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(kd=None), INVALID), (dict(T=0), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(Hq=6, Hk=2), UNSUPPORTED), (dict(L=1025), UNSUPPORTED),
+    (dict(vd=E + 2), MISALIGNED), (dict(o=A), INVALID), (dict(lse=D + 64), INVALID),
+])
+def test_fwd_layer_major_rejects(lib, kw, code):
+    # the layer-major forward validates exactly like moda_fwd
+    assert fwd_lm(lib, **kw) == code
+    assert lib.moda_last_error_detail().decode() != ""
+
+
 def fwd_cc(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.125, o=O, lse=LSE):
     return lib.moda_fwd_depth_cc(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, None)
 
