@@ -331,6 +331,20 @@ MODA_API moda_status moda_bwd(const void* q, const void* k, const void* v, const
                               moda_stream_t stream);
 
 /*
+ * moda_bwd_layer_major -- moda_bwd for moda_fwd_layer_major: kd, vd and the
+ * outputs dkd, dvd are [L, T, Hk, d] (slot l of position t for KV head hk at
+ * [l][t][hk][:]), every other argument as moda_bwd. The same values as
+ * moda_bwd on the packed streams, element for element (only the depth rows'
+ * addresses differ). Errors as moda_bwd.
+ */
+MODA_API moda_status moda_bwd_layer_major(const void* q, const void* k, const void* v,
+                                          const void* kd, const void* vd, const void* o,
+                                          const float* lse, const void* dO, int T, int Hq, int Hk,
+                                          int d, int L, float scale, float* dq, float* dk,
+                                          float* dv, float* dkd, float* dvd, float* delta,
+                                          moda_stream_t stream);
+
+/*
  * moda_bwd_noalloc -- moda_bwd without the caller's workspace; the paper has
  * no counterpart. It is meant for callers that cannot give the library device
  * memory for scratch: code whose device memory is owned by another allocator

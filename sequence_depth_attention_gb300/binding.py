@@ -27,7 +27,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
 EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_depth_write_at", "moda_depth_mass",
            "moda_depth_mass_workspace_bytes", "moda_depth_cache_admit", "moda_kv_proj_write",
            "moda_fwd", "moda_fwd_layer_major", "moda_fwd_depth_cc", "moda_decode",
-           "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_noalloc", "moda_get_device_error",
+           "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_layer_major", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
 _lock = threading.Lock()
@@ -82,6 +82,8 @@ def load():
         lib.moda_fwd_layer_major.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd_layer_major.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
+        lib.moda_bwd_layer_major.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
+        lib.moda_bwd_layer_major.restype = i
         lib.moda_bwd.restype = i
         lib.moda_bwd_noalloc.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 6
         lib.moda_bwd_noalloc.restype = i
@@ -356,36 +358,42 @@ def moda_decode(q, k_cache, v_cache, kd_tok, vd_tok, scale: float, o=None, lse=N
     return o, lse
 
 
-def moda_bwd(q, k, v, kd, vd, o, lse, dO, scale: float, grads=None, delta=None, stream=None):
+def moda_bwd(q, k, v, kd, vd, o, lse, dO, scale: float, grads=None, delta=None, stream=None,
+             layer_major: bool = False):
     """Gradients of moda_fwd. Inputs as passed to moda_fwd plus the forward's
     o and lse and the upstream gradient dO[T,Hq,d] (bf16). Returns fp32
     (dq[T,Hq,d], dk[T,Hk,d], dv[T,Hk,d], dkd[Hk,T,L,d], dvd[Hk,T,L,d]) with
-    the depth gradients in the packed layout (None when L == 0)."""
+    the depth gradients in the packed layout (None when L == 0).
+    layer_major=True calls moda_bwd_layer_major: kd/vd as passed to
+    moda_fwd_layer_major ([L,T,Hk,d]) and dkd/dvd returned in that layout."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
         _need(t, n)
     _need(lse, "lse", torch.float32)
     T, Hq, d = q.shape
     Hk = k.shape[1]
-    L = 0 if kd is None or kd.numel() == 0 else kd.shape[2]
+    L = 0 if kd is None or kd.numel() == 0 else kd.shape[0 if layer_major else 2]
     if L:
         _need(kd, "kd"), _need(vd, "vd")
     dev = q.device
+    dshape = (L, T, Hk, d) if layer_major else (Hk, T, L, d)
     if grads is None:
         f32 = dict(dtype=torch.float32, device=dev)
         grads = (torch.empty((T, Hq, d), **f32), torch.empty((T, Hk, d), **f32),
                  torch.empty((T, Hk, d), **f32),
-                 torch.empty((Hk, T, L, d), **f32) if L else None,
-                 torch.empty((Hk, T, L, d), **f32) if L else None)
+                 torch.empty(dshape, **f32) if L else None,
+                 torch.empty(dshape, **f32) if L else None)
     if delta is None:
         delta = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     dq, dk, dv, dkd, dvd = grads
     for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv"), (delta, "delta")):
         _need(t, n, torch.float32)
-    st = load().moda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kd if L else None),
-                         _ptr(vd if L else None), _ptr(o), _ptr(lse), _ptr(dO), T, Hq, Hk, d, L,
-                         float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkd if L else None),
-                         _ptr(dvd if L else None), _ptr(delta), _stream(stream))
-    _check(st, "moda_bwd")
+    name = "moda_bwd_layer_major" if layer_major else "moda_bwd"
+    st = getattr(load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(kd if L else None),
+                               _ptr(vd if L else None), _ptr(o), _ptr(lse), _ptr(dO), T, Hq, Hk,
+                               d, L, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(dkd if L else None), _ptr(dvd if L else None), _ptr(delta),
+                               _stream(stream))
+    _check(st, name)
     return dq, dk, dv, dkd, dvd
 
 

@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(128)
 bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kd,
                  const __nv_bfloat16* __restrict__ vd, const __nv_bfloat16* __restrict__ dO,
                  const float* __restrict__ lse, const float* __restrict__ delta, int T, int Hq,
-                 int Hk, int L, float scale_log2, float scale, float* __restrict__ dq,
-                 float* __restrict__ dkd, float* __restrict__ dvd) {
+                 int Hk, int L, int layer_major, float scale_log2, float scale,
+                 float* __restrict__ dq, float* __restrict__ dkd, float* __restrict__ dvd) {
   constexpr int E = D / 32;  // columns per lane in phase 2
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,7 +99,10 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
 #pragma unroll
     for (int e = 0; e < E; ++e) dqa[g][e] = 0.f;
 
-  const int64_t slot0 = ((int64_t)hk * T + t) * L;  // packed row of slot 0
+  // row (of D values) of slot l: slot0 + l * lstride, in kd/vd and in dkd/dvd
+  // alike; packed [Hk, T, L, d] or layer-major [L, T, Hk, d]
+  const int64_t slot0 = layer_major ? (int64_t)t * Hk + hk : ((int64_t)hk * T + t) * L;
+  const int64_t lstride = layer_major ? (int64_t)T * Hk : 1;
   for (int l0 = 0; l0 < L; l0 += 32) {
     // ---- phase 1: lane owns slot l0 + lane
     {
@@ -108,8 +111,8 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
 #pragma unroll
       for (int g = 0; g < G; ++g) s[g] = dp[g] = 0.f;
       if (l < L) {
-        const uint4* kr = reinterpret_cast<const uint4*>(kd + (slot0 + l) * D);
-        const uint4* vr = reinterpret_cast<const uint4*>(vd + (slot0 + l) * D);
+        const uint4* kr = reinterpret_cast<const uint4*>(kd + (slot0 + l * lstride) * D);
+        const uint4* vr = reinterpret_cast<const uint4*>(vd + (slot0 + l * lstride) * D);
         for (int ch = 0; ch < D / 8; ++ch) {
           const uint4 kc = __ldg(kr + ch), vc = __ldg(vr + ch);
           const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kc);
@@ -141,7 +144,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
     // ---- phase 2: lane owns columns lane*E .. lane*E+E-1
     const int nl = min(32, L - l0);
     for (int jj = 0; jj < nl; ++jj) {
-      const int64_t prow = slot0 + l0 + jj;
+      const int64_t prow = slot0 + (l0 + jj) * lstride;
       float kdv[E];
       {
         const __nv_bfloat16* kr = kd + prow * D + lane * E;
@@ -200,8 +203,8 @@ cudaError_t launch_depth(const BwdArgs& a, cudaStream_t st) {
   const int64_t pairs = (int64_t)a.Hk * a.T;
   bwd_depth_kernel<D, G><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, (const __nv_bfloat16*)a.vd,
-      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.scale * kLog2e, a.scale,
-      a.dq, a.dkd, a.dvd);
+      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.layer_major,
+      a.scale * kLog2e, a.scale, a.dq, a.dkd, a.dvd);
   return cudaGetLastError();
 }
 

@@ -441,10 +441,11 @@ moda_status moda_fwd_depth_cc(const void* q, const void* k, const void* v, const
   return ok();
 }
 
-moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd, const void* vd,
-                     const void* o, const float* lse, const void* dO, int T, int Hq, int Hk,
-                     int d, int L, float scale, float* dq, float* dk, float* dv, float* dkd,
-                     float* dvd, float* delta, moda_stream_t stream) {
+static moda_status bwd_impl(const void* q, const void* k, const void* v, const void* kd,
+                            const void* vd, const void* o, const float* lse, const void* dO, int T,
+                            int Hq, int Hk, int d, int L, float scale, float* dq, float* dk,
+                            float* dv, float* dkd, float* dvd, float* delta, moda_stream_t stream,
+                            int layer_major) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
     return fail(MODA_ERR_INVALID_ARG, "NULL input, output or workspace pointer");
   if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
@@ -485,12 +486,30 @@ moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd
   a.T = T; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G; a.scale = scale;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dkd = L ? dkd : nullptr; a.dvd = L ? dvd : nullptr;
   a.delta = delta;
+  a.layer_major = layer_major;
   int dev;
   moda_status st = device_state(&dev, &a.err, &a.num_sms);
   if (st != MODA_OK) return st;
   cudaError_t e = moda::launch_bwd(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_bwd launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+moda_status moda_bwd(const void* q, const void* k, const void* v, const void* kd, const void* vd,
+                     const void* o, const float* lse, const void* dO, int T, int Hq, int Hk,
+                     int d, int L, float scale, float* dq, float* dk, float* dv, float* dkd,
+                     float* dvd, float* delta, moda_stream_t stream) {
+  return bwd_impl(q, k, v, kd, vd, o, lse, dO, T, Hq, Hk, d, L, scale, dq, dk, dv, dkd, dvd, delta,
+                  stream, 0);
+}
+
+moda_status moda_bwd_layer_major(const void* q, const void* k, const void* v, const void* kd,
+                                 const void* vd, const void* o, const float* lse, const void* dO,
+                                 int T, int Hq, int Hk, int d, int L, float scale, float* dq,
+                                 float* dk, float* dv, float* dkd, float* dvd, float* delta,
+                                 moda_stream_t stream) {
+  return bwd_impl(q, k, v, kd, vd, o, lse, dO, T, Hq, Hk, d, L, scale, dq, dk, dv, dkd, dvd, delta,
+                  stream, 1);
 }
 
 size_t moda_decode_workspace_bytes(int Tctx, int Hq, int d) {

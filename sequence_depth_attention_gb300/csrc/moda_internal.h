@@ -37,6 +37,7 @@ struct BwdArgs {
   float* delta;                              // [T, Hq] caller workspace
   unsigned int* err;                         // device error word of the current device
   int num_sms;
+  int layer_major;  // kd/vd and dkd/dvd as [L, T, Hk, d] instead of packed
 };
 
 // Arguments of one decode call after validation on the host.

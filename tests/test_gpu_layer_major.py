@@ -1,15 +1,17 @@
-"""The forward on layer-major depth K/V (moda_fwd_layer_major): kd/vd
-[L,T,Hk,d] as the layers wrote them, each depth block gathered by the
-forward's tensor-memory-accelerator copies (the chunk-aware grouping of
-Mixture-of-Depths Attention, Sec. 3.2, Fig. 4, without a relayout pass),
-against the fp64 oracle, which reads the same layer-major tensors."""
+"""The forward and backward on layer-major depth K/V (moda_fwd_layer_major,
+moda_bwd_layer_major): kd/vd [L,T,Hk,d] as the layers wrote them, each depth
+block gathered by the forward's tensor-memory-accelerator copies (the
+chunk-aware grouping of Mixture-of-Depths Attention, Sec. 3.2, Fig. 4,
+without a relayout pass), against the fp64 oracle, which reads the same
+layer-major tensors."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import sequence_depth_attention_gb300 as moda
 from sequence_depth_attention_gb300 import inputs as wl
-from sequence_depth_attention_gb300.inputs import Workload, make_inputs
+from sequence_depth_attention_gb300.inputs import Workload, bf16_bits, make_inputs
 
 import gpu_common as gc
 
@@ -96,3 +98,58 @@ def test_layer_major_prefix_of_a_larger_buffer():
     torch.cuda.synchronize()
     eo, el = gc.compare(x, w.scale, o.float().cpu().numpy(), lse.cpu().numpy())
     assert eo <= gc.TOL_O and el <= gc.TOL_LSE
+
+
+# ---------------------------------------------------------------- backward
+BWD_REL = 1e-2  # as the packed backward's tests: 1 % of each gradient's scale
+
+
+def _bwd_check(name, got, ref):
+    scale = max(float(np.max(np.abs(ref))), 1e-30)
+    err = float(np.max(np.abs(got - ref)))
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    assert err <= BWD_REL * scale, f"{name}: max err {err:.3e} > {BWD_REL} * {scale:.3e}"
+
+
+@pytest.mark.parametrize("w", [Workload("lm-bwd-T300-G4", T=300, Hq=8, Hk=2, d=128, L=24, seed=5),
+                               Workload("lm-bwd-T200-G1-d64", T=200, Hq=3, Hk=3, d=64, L=33),
+                               Workload("lm-bwd-T127-G8", T=127, Hq=16, Hk=2, d=128, L=7)],
+                         ids=lambda w: w.name)
+def test_layer_major_backward_matches_oracle(w):
+    """moda_fwd_layer_major then moda_bwd_layer_major: every gradient against
+    the oracle backward, dkd/dvd compared in their own [L,T,Hk,d] layout."""
+    x = make_inputs(w)
+    g = torch.Generator().manual_seed(77)
+    dO = torch.randn((w.T, w.Hq, w.d), generator=g).to(torch.bfloat16)
+    q, k, v, kd, vd, dOg = (t.cuda() for t in (x["q"], x["k"], x["v"], x["kd"], x["vd"], dO))
+    o, lse = moda.moda_fwd_layer_major(q, k, v, kd, vd, w.scale)
+    grads = moda.moda_bwd(q, k, v, kd, vd, o, lse, dOg, w.scale, layer_major=True)
+    torch.cuda.synchronize()
+    assert moda.moda_get_device_error() == 0
+    b = {n: bf16_bits(t) for n, t in x.items()}
+    ref = oracle.backward(b["q"], b["k"], b["v"], b["kd"], b["vd"], bf16_bits(dO), w.scale,
+                          nthreads=gc.NTHREADS)
+    for name, gg, r in zip(("dq", "dk", "dv", "dkd", "dvd"), grads, ref):
+        _bwd_check(f"{w.name}.{name}", gg.cpu().numpy(), r)
+
+
+def test_layer_major_backward_equals_packed_backward():
+    """Same o, lse and dO into moda_bwd (packed streams) and
+    moda_bwd_layer_major: only the depth rows' addresses differ, so every
+    gradient is bit-identical (dkd/dvd after the relayout)."""
+    w = Workload("lm-bwd-eq", T=700, Hq=16, Hk=4, d=128, L=20, seed=3)
+    x = {n: t.cuda() for n, t in make_inputs(w).items()}
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dO = torch.randn((w.T, w.Hq, w.d), generator=g, device="cuda").to(torch.bfloat16)
+    kd = moda.moda_pack_depth(x["kd"])
+    vd = moda.moda_pack_depth(x["vd"])
+    o, lse = moda.moda_fwd(x["q"], x["k"], x["v"], kd, vd, w.scale)
+    gp = moda.moda_bwd(x["q"], x["k"], x["v"], kd, vd, o, lse, dO, w.scale)
+    gl = moda.moda_bwd(x["q"], x["k"], x["v"], x["kd"], x["vd"], o, lse, dO, w.scale,
+                       layer_major=True)
+    torch.cuda.synchronize()
+    assert moda.moda_get_device_error() == 0
+    for a, b_ in zip(gp[:3], gl[:3]):
+        assert torch.equal(a, b_)
+    for a, b_ in zip(gp[3:], gl[3:]):
+        assert torch.equal(a.permute(2, 1, 0, 3), b_)
