@@ -20,7 +20,9 @@
 // two blocks ahead of the P.V cursor).
 // Depth blocks belong to one tile: as in the d = 128 kernel, each of its
 // softmax warps owns one 32-row word of the block, filled with the next packed
-// depth rows of the warp's own positions. A tile's depth blocks are its own
+// depth rows of the warp's own positions (or, from layer-major depth tensors,
+// gathered by a 4-D copy box of its PW positions x 32/PW slots). A tile's
+// depth blocks are its own
 // (A's first, then B's in the pair's schedule); the last sequence block may be
 // used by both tiles. Every K/V stage is
 // released by two arrivals per block, one per tile: the MMA commit of a tile

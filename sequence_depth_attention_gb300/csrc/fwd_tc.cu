@@ -17,9 +17,13 @@
 //     softmax warp owns one 32-row word of every depth block, filled with the
 //     next packed rows of its own positions, so a row keeps depth columns of
 //     its own warp's word only (the block-diagonal mask of Sec. 3.3 within
-//     that word). An exact online softmax does not depend on block order, so
-//     depth blocks are spread evenly among the sequence blocks: each tile
-//     streams its depth rows from HBM over its lifetime;
+//     that word). From layer-major depth tensors [L][T][Hk][d] (the order the
+//     layers write them) the copy engine gathers the same word shape itself:
+//     a 4-D box of the warp's PW positions x 32/PW slots, so the chunk-aware
+//     grouping needs no relayout pass; a row's columns are then every PW-th
+//     one. An exact online softmax does not depend on block order, so depth
+//     blocks are spread evenly among the sequence blocks: each tile streams
+//     its depth rows from HBM over its lifetime;
 //   * sequence blocks of 128 keys, the grouped causal mask key <= p0 + r/G
 //     applied only on blocks that reach past p0;
 //   * one running state per row: max m (log2 units), sum l, and the
