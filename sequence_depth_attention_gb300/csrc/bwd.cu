@@ -10,8 +10,9 @@
 // Four launches, every output row with one owner (no atomics):
 //   1. delta     D[t,h] = <dO[t,h], o[t,h]>                   (caller workspace)
 //   2. depth     one warp per (hk, t): the G rows x L slots of that position
-//                on CUDA cores -> dkd, dvd (packed layout) and dq's depth
-//                share, written as dq's initial value
+//                on CUDA cores -> dkd, dvd (in the layout of kd, vd: packed
+//                or layer-major) and dq's depth share, written as dq's
+//                initial value
 //   3. dq        tcgen05 (bwd_dq_tc.cu), added to dq
 //   4. dk/dv     tcgen05 (bwd_dkdv_tc.cu)
 // All gradients are fp32.
@@ -49,8 +50,12 @@ bwd_delta_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __res
 // ---------------------------------------------------------------- 2. depth
 // Per-warp shared state; 16-byte aligned so that every warp's q/dO rows take
 // 16-byte accesses.
-template <int D, int G>
+template <int D, int G, bool LM>
 struct alignas(16) DepthWarpSmem {
+  // layer-major only: the chunk's 32 kd and vd rows, 16-byte piece c of row r
+  // at c ^ (r % (D/8))
+  uint4 kr[LM ? 32 : 1][D / 8];
+  uint4 vr[LM ? 32 : 1][D / 8];
   __nv_bfloat16 qs[G][D];
   __nv_bfloat16 ds_[G][D];  // dO rows
   float P[G][32];
@@ -59,21 +64,26 @@ struct alignas(16) DepthWarpSmem {
   float Dd[G];
 };
 
-// One warp per (hk, t). Phase 1: lane l computes, for its slot and every head
-// g of the group, p and ds (full-length dot products). Phase 2: lanes split
-// the d columns and walk the 32 slots of the chunk, producing dvd and dkd
-// rows (coalesced) and accumulating dq's depth share.
-template <int D, int G>
+// One warp per (hk, t), 32 slots at a time. Phase 1: lane l computes, for its
+// slot and every head g of the group, p and ds (full-length dot products).
+// Phase 2: lanes split the d columns and walk the 32 slots of the chunk,
+// producing dvd and dkd rows (coalesced) and accumulating dq's depth share.
+// Packed depth (LM false): a position's slots are adjacent rows, and each
+// lane reads its own row straight from global memory. Layer-major (LM true):
+// the slots lie T*Hk rows apart, so the chunk's kd and vd rows are first
+// staged in shared memory with coalesced 16-byte loads, each lane then reading
+// its row in a swizzled order that puts the 32 lanes' rows in distinct banks.
+template <int D, int G, bool LM>
 __global__ void __launch_bounds__(128)
 bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kd,
                  const __nv_bfloat16* __restrict__ vd, const __nv_bfloat16* __restrict__ dO,
                  const float* __restrict__ lse, const float* __restrict__ delta, int T, int Hq,
-                 int Hk, int L, int layer_major, float scale_log2, float scale,
-                 float* __restrict__ dq, float* __restrict__ dkd, float* __restrict__ dvd) {
+                 int Hk, int L, float scale_log2, float scale, float* __restrict__ dq,
+                 float* __restrict__ dkd, float* __restrict__ dvd) {
   constexpr int E = D / 32;  // columns per lane in phase 2
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DepthWarpSmem<D, G>& sm = reinterpret_cast<DepthWarpSmem<D, G>*>(smem_raw)[warp];
+  DepthWarpSmem<D, G, LM>& sm = reinterpret_cast<DepthWarpSmem<D, G, LM>*>(smem_raw)[warp];
   const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
   if (pair >= (int64_t)Hk * T) return;
   const int hk = (int)(pair / T), t = (int)(pair - (int64_t)hk * T);
@@ -101,9 +111,27 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
 
   // row (of D values) of slot l: slot0 + l * lstride, in kd/vd and in dkd/dvd
   // alike; packed [Hk, T, L, d] or layer-major [L, T, Hk, d]
-  const int64_t slot0 = layer_major ? (int64_t)t * Hk + hk : ((int64_t)hk * T + t) * L;
-  const int64_t lstride = layer_major ? (int64_t)T * Hk : 1;
+  const int64_t slot0 = LM ? (int64_t)t * Hk + hk : ((int64_t)hk * T + t) * L;
+  const int64_t lstride = LM ? (int64_t)T * Hk : 1;
+  constexpr int CH = D / 8;  // 16-byte pieces per row
   for (int l0 = 0; l0 < L; l0 += 32) {
+    const int nl = min(32, L - l0);
+    if constexpr (LM) {
+      // ---- stage the chunk's rows
+#pragma unroll 4
+      for (int idx = lane; idx < 32 * CH; idx += 32) {
+        const int r = idx / CH, c = idx % CH;
+        uint4 kc = make_uint4(0u, 0u, 0u, 0u), vc = kc;
+        if (r < nl) {
+          const int64_t row = slot0 + (int64_t)(l0 + r) * lstride;
+          kc = __ldg(reinterpret_cast<const uint4*>(kd + row * D) + c);
+          vc = __ldg(reinterpret_cast<const uint4*>(vd + row * D) + c);
+        }
+        sm.kr[r][c ^ (r & (CH - 1))] = kc;
+        sm.vr[r][c ^ (r & (CH - 1))] = vc;
+      }
+      __syncwarp();
+    }
     // ---- phase 1: lane owns slot l0 + lane
     {
       const int l = l0 + lane;
@@ -111,10 +139,17 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
 #pragma unroll
       for (int g = 0; g < G; ++g) s[g] = dp[g] = 0.f;
       if (l < L) {
-        const uint4* kr = reinterpret_cast<const uint4*>(kd + (slot0 + l * lstride) * D);
-        const uint4* vr = reinterpret_cast<const uint4*>(vd + (slot0 + l * lstride) * D);
-        for (int ch = 0; ch < D / 8; ++ch) {
-          const uint4 kc = __ldg(kr + ch), vc = __ldg(vr + ch);
+        const uint4* kg = reinterpret_cast<const uint4*>(kd + (slot0 + l * lstride) * D);
+        const uint4* vg = reinterpret_cast<const uint4*>(vd + (slot0 + l * lstride) * D);
+        for (int ch = 0; ch < CH; ++ch) {
+          uint4 kc, vc;
+          if constexpr (LM) {
+            kc = sm.kr[lane][ch ^ (lane & (CH - 1))];
+            vc = sm.vr[lane][ch ^ (lane & (CH - 1))];
+          } else {
+            kc = __ldg(kg + ch);
+            vc = __ldg(vg + ch);
+          }
           const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kc);
           const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vc);
 #pragma unroll
@@ -142,12 +177,17 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
     }
     __syncwarp();
     // ---- phase 2: lane owns columns lane*E .. lane*E+E-1
-    const int nl = min(32, L - l0);
     for (int jj = 0; jj < nl; ++jj) {
       const int64_t prow = slot0 + (l0 + jj) * lstride;
       float kdv[E];
       {
-        const __nv_bfloat16* kr = kd + prow * D + lane * E;
+        // layer-major: columns lane*E.. lie in piece (lane*E)/8 of staged row
+        // jj, at its swizzled place
+        const int col = lane * E;
+        const __nv_bfloat16* kr =
+            LM ? reinterpret_cast<const __nv_bfloat16*>(&sm.kr[jj][(col >> 3) ^ (jj & (CH - 1))]) +
+                     (col & 7)
+               : kd + prow * D + col;
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kr + e));
@@ -194,18 +234,23 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
   }
 }
 
-template <int D, int G>
-cudaError_t launch_depth(const BwdArgs& a, cudaStream_t st) {
-  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G>);
-  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G>,
+template <int D, int G, bool LM>
+cudaError_t launch_depth_layout(const BwdArgs& a, cudaStream_t st) {
+  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G, LM>);
+  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G, LM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs = (int64_t)a.Hk * a.T;
-  bwd_depth_kernel<D, G><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
+  bwd_depth_kernel<D, G, LM><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, (const __nv_bfloat16*)a.vd,
-      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.layer_major,
-      a.scale * kLog2e, a.scale, a.dq, a.dkd, a.dvd);
+      (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.scale * kLog2e, a.scale,
+      a.dq, a.dkd, a.dvd);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_depth(const BwdArgs& a, cudaStream_t st) {
+  return a.layer_major ? launch_depth_layout<D, G, true>(a, st) : launch_depth_layout<D, G, false>(a, st);
 }
 
 template <int D>
