@@ -299,6 +299,23 @@ MODA_API moda_status moda_decode(const void* q, const void* k_cache, const void*
                                  size_t workspace_bytes, moda_stream_t stream);
 
 /*
+ * moda_decode_strided -- moda_decode with the token's depth slots at any
+ * spacing: slot l of KV head hk is the d values at
+ * kd_tok + l*depth_slot_stride + hk*depth_hk_stride (elements; the same for
+ * vd_tok). For the layer-major depth tensors of moda_fwd_layer_major,
+ * [L, T, Hk, d], position t's slots are kd + t*Hk*d with
+ * depth_slot_stride = T*Hk*d and depth_hk_stride = d. Both strides >= d and
+ * multiples of 8 (depth_hk_stride is not used when Hk == 1); every other
+ * argument, the arithmetic and the errors as moda_decode.
+ */
+MODA_API moda_status moda_decode_strided(const void* q, const void* k_cache, const void* v_cache,
+                                         const void* kd_tok, const void* vd_tok,
+                                         long long depth_slot_stride, long long depth_hk_stride,
+                                         int Tctx, int Hq, int Hk, int d, int L, float scale,
+                                         void* o, float* lse, float* workspace,
+                                         size_t workspace_bytes, moda_stream_t stream);
+
+/*
  * moda_bwd -- gradients of moda_fwd with respect to all of its inputs. The
  * pages time the fused operator forward + backward (Table 2, Table 7) without
  * writing the backward out; this is the chain rule through the joint softmax

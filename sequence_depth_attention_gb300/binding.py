@@ -27,6 +27,7 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
 EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_depth_write_at", "moda_depth_mass",
            "moda_depth_mass_workspace_bytes", "moda_depth_cache_admit", "moda_kv_proj_write",
            "moda_fwd", "moda_fwd_layer_major", "moda_fwd_depth_cc", "moda_decode",
+           "moda_decode_strided",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_layer_major", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
 
@@ -75,6 +76,9 @@ def load():
         lib.moda_decode.argtypes = [vp] * 5 + [ctypes.c_longlong] + [i] * 5 + [f, vp, vp, vp,
                                                                            ctypes.c_size_t, vp]
         lib.moda_decode.restype = i
+        lib.moda_decode_strided.argtypes = [vp] * 5 + [ctypes.c_longlong] * 2 + [i] * 5 + [
+            f, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.moda_decode_strided.restype = i
         lib.moda_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd_depth_cc.restype = i
         lib.moda_fwd_depth_cc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
@@ -325,24 +329,28 @@ def moda_decode_workspace_bytes(Tctx: int, Hq: int, d: int) -> int:
 def moda_decode(q, k_cache, v_cache, kd_tok, vd_tok, scale: float, o=None, lse=None,
                 workspace=None, stream=None):
     """One decoding step. q[Hq,d]; k_cache/v_cache[Tctx,Hk,d]; kd_tok/vd_tok
-    [Hk,L,d] views whose rows [L,d] are contiguous (stride(0) may be larger,
-    e.g. kd_packed[:, t]) or None when L == 0. Returns (o[Hq,d], lse[Hq])."""
+    [Hk,L,d] bf16 views with contiguous rows of d values (e.g. kd_packed[:, t],
+    or kd_layer_major[:, t].transpose(0, 1) for [L,T,Hk,d] tensors) or None
+    when L == 0. Views whose [L,d] blocks are contiguous go to moda_decode,
+    others to moda_decode_strided. Returns (o[Hq,d], lse[Hq])."""
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n)
     Hq, d = q.shape
     Tctx, Hk, _ = k_cache.shape
     if kd_tok is None or kd_tok.numel() == 0:
-        L, stride = 0, 0
+        L, stride, slot_stride = 0, 0, 0
         kd_tok = vd_tok = None
     else:
         L = kd_tok.shape[1]
         for t, n in ((kd_tok, "kd_tok"), (vd_tok, "vd_tok")):
             if not t.is_cuda or t.dtype != torch.bfloat16 or t.shape != (Hk, L, d) or \
-                    t.stride(2) != 1 or (L > 1 and t.stride(1) != d):
-                raise ValueError(f"{n}: expected a bf16 CUDA view [Hk,L,d] with contiguous [L,d] rows")
+                    t.stride(2) != 1:
+                raise ValueError(f"{n}: expected a bf16 CUDA view [Hk,L,d] with contiguous rows")
         stride = kd_tok.stride(0) if Hk > 1 else L * d  # one head: the stride is never used
-        if Hk > 1 and kd_tok.stride(0) != vd_tok.stride(0):
-            raise ValueError("kd_tok and vd_tok must have the same KV-head stride")
+        slot_stride = kd_tok.stride(1) if L > 1 else d
+        if (Hk > 1 and kd_tok.stride(0) != vd_tok.stride(0)) or \
+                (L > 1 and kd_tok.stride(1) != vd_tok.stride(1)):
+            raise ValueError("kd_tok and vd_tok must have the same strides")
     if o is None:
         o = torch.empty((Hq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -350,11 +358,18 @@ def moda_decode(q, k_cache, v_cache, kd_tok, vd_tok, scale: float, o=None, lse=N
     need = moda_decode_workspace_bytes(Tctx, Hq, d)
     if workspace is None:
         workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=q.device)
-    st = load().moda_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kd_tok), _ptr(vd_tok),
-                            int(stride), Tctx, Hq, Hk, d, L, float(scale), _ptr(o), _ptr(lse),
-                            _ptr(workspace), workspace.numel() * workspace.element_size(),
-                            _stream(stream))
-    _check(st, "moda_decode")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if slot_stride in (0, d) and (Hk == 1 or stride >= L * d):
+        st = load().moda_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kd_tok), _ptr(vd_tok),
+                                int(stride), Tctx, Hq, Hk, d, L, float(scale), _ptr(o), _ptr(lse),
+                                _ptr(workspace), ws_bytes, _stream(stream))
+        _check(st, "moda_decode")
+    else:
+        st = load().moda_decode_strided(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kd_tok),
+                                        _ptr(vd_tok), int(slot_stride), int(stride), Tctx, Hq, Hk,
+                                        d, L, float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                                        ws_bytes, _stream(stream))
+        _check(st, "moda_decode_strided")
     return o, lse
 
 

@@ -346,7 +346,7 @@ cudaError_t launch_split(const DecodeArgs& a, int nsplit, int kps, cudaStream_t 
   }
   if (a.L > 0) {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.L, (uint64_t)a.Hk};
-    const uint64_t str[2] = {row, (uint64_t)a.depth_hk_stride * 2};
+    const uint64_t str[2] = {(uint64_t)a.depth_slot_stride * 2, (uint64_t)a.depth_hk_stride * 2};
     const uint32_t box[3] = {64, kKB, 1};
     if (encode_bf16_sw128(&tkd, a.kd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_bf16_sw128(&tvd, a.vd, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;

@@ -517,10 +517,13 @@ size_t moda_decode_workspace_bytes(int Tctx, int Hq, int d) {
   return (size_t)(moda::decode_num_splits(Tctx) + 1) * Hq * (d + 2) * sizeof(float);
 }
 
-moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
-                        const void* kd_tok, const void* vd_tok, long long depth_hk_stride,
-                        int Tctx, int Hq, int Hk, int d, int L, float scale, void* o, float* lse,
-                        float* workspace, size_t workspace_bytes, moda_stream_t stream) {
+// slot_stride == 0: moda_decode's [L, d] blocks (consecutive slots d apart,
+// blocks at least L*d apart); otherwise any slot and KV-head strides.
+static moda_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                               const void* kd_tok, const void* vd_tok, long long slot_stride,
+                               long long depth_hk_stride, int Tctx, int Hq, int Hk, int d, int L,
+                               float scale, void* o, float* lse, float* workspace,
+                               size_t workspace_bytes, moda_stream_t stream) {
   if (!q || !k_cache || !v_cache || !o || !workspace)
     return fail(MODA_ERR_INVALID_ARG, "NULL q, cache, o or workspace");
   if (Tctx < 1) return fail(MODA_ERR_INVALID_ARG, "Tctx = %d < 1", Tctx);
@@ -536,9 +539,18 @@ moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
     return fail(MODA_ERR_UNSUPPORTED, "G = Hq/Hk = %d (supported: 1, 2, 4, 8, 16)", G);
   if (Tctx > (1 << 24)) return fail(MODA_ERR_UNSUPPORTED, "Tctx = %d > 2^24", Tctx);
   if (L > 1024) return fail(MODA_ERR_UNSUPPORTED, "L = %d > 1024", L);
-  if (L > 0 && (depth_hk_stride < (long long)L * d || depth_hk_stride % 8 != 0))
-    return fail(MODA_ERR_INVALID_ARG, "depth_hk_stride = %lld must be >= L*d and a multiple of 8",
-                depth_hk_stride);
+  if (slot_stride == 0) {
+    if (L > 0 && (depth_hk_stride < (long long)L * d || depth_hk_stride % 8 != 0))
+      return fail(MODA_ERR_INVALID_ARG, "depth_hk_stride = %lld must be >= L*d and a multiple of 8",
+                  depth_hk_stride);
+    slot_stride = d;
+  } else if (L > 0 && (slot_stride < d || slot_stride % 8 != 0 ||
+                       (Hk > 1 && (depth_hk_stride < d || depth_hk_stride % 8 != 0)))) {
+    return fail(MODA_ERR_INVALID_ARG,
+                "depth strides (slot %lld, KV head %lld) must be >= d and multiples of 8",
+                slot_stride, depth_hk_stride);
+  }
+  if (Hk == 1) depth_hk_stride = (long long)L * d;  // never used to step between heads
   if (workspace_bytes < moda_decode_workspace_bytes(Tctx, Hq, d))
     return fail(MODA_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes,
                 moda_decode_workspace_bytes(Tctx, Hq, d));
@@ -546,7 +558,8 @@ moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
   for (const void* p : al)
     if (p && !aligned16(p)) return fail(MODA_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
   const size_t qb = (size_t)Hq * d * 2, cb = (size_t)Tctx * Hk * d * 2;
-  const size_t db = L ? ((size_t)(Hk - 1) * depth_hk_stride + (size_t)L * d) * 2 : 0;
+  const size_t db =
+      L ? ((size_t)(Hk - 1) * depth_hk_stride + (size_t)(L - 1) * slot_stride + (size_t)d) * 2 : 0;
   const void* ins[] = {q, k_cache, v_cache, L ? kd_tok : nullptr, L ? vd_tok : nullptr};
   const size_t insz[] = {qb, cb, cb, db, db};
   void* outs[] = {o, lse, workspace};
@@ -562,6 +575,7 @@ moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
   moda::DecodeArgs a{};
   a.q = q; a.k = k_cache; a.v = v_cache; a.kd = L ? kd_tok : nullptr; a.vd = L ? vd_tok : nullptr;
   a.depth_hk_stride = depth_hk_stride;
+  a.depth_slot_stride = slot_stride;
   a.Tctx = Tctx; a.Hq = Hq; a.Hk = Hk; a.d = d; a.L = L; a.G = G; a.scale = scale;
   a.o = o; a.lse = lse; a.work = workspace;
   int dev;
@@ -570,6 +584,26 @@ moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
   cudaError_t e = moda::launch_decode(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(MODA_ERR_CUDA, "moda_decode launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+moda_status moda_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const void* kd_tok, const void* vd_tok, long long depth_hk_stride,
+                        int Tctx, int Hq, int Hk, int d, int L, float scale, void* o, float* lse,
+                        float* workspace, size_t workspace_bytes, moda_stream_t stream) {
+  return decode_impl(q, k_cache, v_cache, kd_tok, vd_tok, 0, depth_hk_stride, Tctx, Hq, Hk, d, L,
+                     scale, o, lse, workspace, workspace_bytes, stream);
+}
+
+moda_status moda_decode_strided(const void* q, const void* k_cache, const void* v_cache,
+                                const void* kd_tok, const void* vd_tok,
+                                long long depth_slot_stride, long long depth_hk_stride, int Tctx,
+                                int Hq, int Hk, int d, int L, float scale, void* o, float* lse,
+                                float* workspace, size_t workspace_bytes, moda_stream_t stream) {
+  if (L > 0 && depth_slot_stride < 1)
+    return fail(MODA_ERR_INVALID_ARG, "depth_slot_stride = %lld < 1", depth_slot_stride);
+  return decode_impl(q, k_cache, v_cache, kd_tok, vd_tok, L > 0 ? depth_slot_stride : d,
+                     depth_hk_stride, Tctx, Hq, Hk, d, L, scale, o, lse, workspace,
+                     workspace_bytes, stream);
 }
 
 moda_status moda_selftest_wait_timeout(int timeout_ms, moda_stream_t stream) {

@@ -44,6 +44,7 @@ struct BwdArgs {
 struct DecodeArgs {
   const void *q, *k, *v, *kd, *vd;  // q [Hq,d]; k/v cache [Tctx,Hk,d]; depth slots (see stride)
   int64_t depth_hk_stride;           // elements between the [L,d] blocks of consecutive KV heads
+  int64_t depth_slot_stride;         // elements between consecutive slots of one KV head
   int Tctx, Hq, Hk, d, L, G;
   float scale;
   void* o;                           // [Hq,d] bf16

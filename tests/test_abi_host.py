@@ -261,3 +261,24 @@ def test_cache_admit_rejects(lib, kw, code):
 ])
 def test_depth_write_at_rejects(lib, args, code):
     assert lib.moda_depth_write_at(*args, None) == code
+
+
+def _dec_strided(lib, q=A, kc=B, vc=C, kt=D, vt=E, slot=100 * 2 * 64, hks=64, T=100, Hq=4, Hk=2,
+                 d=64, L=4, scale=0.125, o=O, lse=LSE, ws=0x78000000, wsb=1 << 20):
+    lib.moda_decode_strided.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_longlong] * 2 + [
+        ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_size_t, ctypes.c_void_p]
+    return lib.moda_decode_strided(q, kc, vc, kt, vt, slot, hks, T, Hq, Hk, d, L, scale, o, lse, ws,
+                                   wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(slot=0), INVALID), (dict(slot=32), INVALID), (dict(slot=68), INVALID),
+    (dict(hks=32), INVALID), (dict(hks=66), INVALID), (dict(q=None), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(L=1025), UNSUPPORTED), (dict(kt=D + 2), MISALIGNED),
+    (dict(o=D + 12800 * 2), INVALID),   # o inside the strided depth slots
+])
+def test_decode_strided_rejects(lib, kw, code):
+    # the strided decode validates its strides and otherwise as moda_decode
+    assert _dec_strided(lib, **kw) == code
+    assert lib.moda_last_error_detail().decode() != ""

@@ -19,13 +19,17 @@ def _built():
     gc.ensure_built()
 
 
-def decode_and_compare(w, packed_view=False, device_inputs=False):
+def decode_and_compare(w, packed_view=False, device_inputs=False, layer_major_view=False):
     x = make_inputs(w, device="cuda" if device_inputs else "cpu")
     t = w.T - 1
     q = x["q"][t].cuda().contiguous()
     kc, vc = x["k"].cuda(), x["v"].cuda()
     if w.L == 0:
         kt = vt = None
+    elif layer_major_view:
+        # the layer-major tensors in place: slot stride T*Hk*d, KV-head stride d
+        kdl, vdl = x["kd"].cuda(), x["vd"].cuda()
+        kt, vt = kdl[:, t].transpose(0, 1), vdl[:, t].transpose(0, 1)
     elif packed_view:
         kp = moda.moda_pack_depth(x["kd"].cuda())
         vp = moda.moda_pack_depth(x["vd"].cuda())
@@ -61,6 +65,16 @@ CASES = [
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_decode_vs_oracle(w):
     decode_and_compare(w)
+
+
+@pytest.mark.parametrize("w", [Workload("dec-lm-T777-G4", T=777, Hq=8, Hk=2, d=128, L=13, seed=6),
+                               Workload("dec-lm-T300-G1-d64", T=300, Hq=3, Hk=3, d=64, L=70, seed=7),
+                               Workload("dec-lm-T129-G16", T=129, Hq=16, Hk=1, d=128, L=5, seed=8)],
+                         ids=lambda w: w.name)
+def test_decode_reads_layer_major_tensors_in_place(w):
+    """moda_decode_strided on [L,T,Hk,d] depth tensors, the token's slots
+    T*Hk*d elements apart (the layout moda_fwd_layer_major reads)."""
+    decode_and_compare(w, layer_major_view=True)
 
 
 def test_decode_reads_packed_stream_in_place():
