@@ -110,6 +110,8 @@ struct alignas(8) Barriers {
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t t_full[kTileRing], t_empty[kTileRing];
   uint64_t mma_done, mma_done_pv;
+  uint64_t o_staged;  // a tile's O rows sit in the Q region (128 softmax arrivals)
+  uint64_t o_free;    // the TMA store of that O has read the Q region
   int tile_ring[kTileRing];
   uint32_t tmem_base;
   int abort;
@@ -120,8 +122,6 @@ struct Params {
   int T, Hq, Hk, L, lgG, ntiles, total, head_major;
   int depth_lm;  // depth K/V layer-major [L, T, Hk, d] (else packed [Hk, T, L, d])
   float scale_log2;
-  __nv_bfloat16* o;
-  int o_v8;  // o is 32-byte aligned: rows go out in 32-byte stores
   float* lse;
   unsigned int* err;
   unsigned int* queue;  // {next tile, CTAs finished}
@@ -193,7 +193,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKd,
-                   const __grid_constant__ CUtensorMap tmVd, const Params p) {
+                   const __grid_constant__ CUtensorMap tmVd, const __grid_constant__ CUtensorMap tmO,
+                   const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -211,6 +212,8 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     bars->abort = 0;
     mbar_init(smem_u32(&bars->q_full), 1);
     mbar_init(smem_u32(&bars->q_tmem), 128);
+    mbar_init(smem_u32(&bars->o_staged), 128);
+    mbar_init(smem_u32(&bars->o_free), 1);
     for (int s = 0; s < 4; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
       mbar_init(smem_u32(&bars->k_empty[s]), 1);
@@ -235,6 +238,7 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
     if (p.L) {
       tma_prefetch_desc(&tmKd);
       tma_prefetch_desc(&tmVd);
@@ -268,6 +272,25 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint64_t pol_once = l2_policy_evict_first();
     int g = 0;   // blocks issued so far, over all tiles
     int nq = 0;  // Q loads issued
+    int ntile = 0;            // tiles taken (K producer)
+    int tile_even = 0, tile_odd = 0;  // the last two tiles' numbers (K producer)
+    // The O of tile kk: the softmax warps stage its rows in the Q region (in
+    // the o tensor map's box layout) once the next tile's Q is in TMEM; one
+    // TMA store per 64-column half writes them out, and the region is free
+    // again once the store has read it.
+    auto store_o = [&](int kk) -> bool {
+      if (!warp_wait(smem_u32(&bars->o_staged), kk & 1, abort)) return false;
+      if (leader) {
+        Tile t;
+        t.set((kk & 1) ? tile_odd : tile_even, p);
+        for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(&tmO, sQ + c * C::kBoxBytes, c * 64, t.hk * G, t.p0);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(smem_u32(&bars->o_free));
+      }
+      __syncwarp();
+      return true;
+    };
     bool ok = true;
     for (int k = 0; ok; ++k) {
       int o;
@@ -290,8 +313,12 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tl.set(o, p);
       if (is_k) {
         // Q of this tile, once the softmax warps have copied the previous Q
-        // into TMEM (the Q region is free again)
+        // into TMEM and the O of tile k-2, staged in the Q region after that
+        // copy, has been read out of it
         if (k > 0 && !warp_wait(smem_u32(&bars->q_tmem), (k - 1) & 1, abort)) break;
+        if (k >= 2 && !store_o(k - 2)) break;
+        if (k & 1) tile_odd = o; else tile_even = o;
+        ntile = k + 1;
         if (leader) {
           const uint32_t qb = smem_u32(&bars->q_full);
           mbar_arrive_expect_tx(qb, C::kQBytes);
@@ -339,8 +366,15 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         __syncwarp();
       }
     }
-    // drain: every copy this warp issued has landed before smem is released
+    // the last two tiles' O (nothing to wait for after a timeout: the
+    // bounded waits return at once once the abort flag is up)
+    if (is_k)
+      for (int kk = max(0, ntile - 2); kk < ntile && !*abort; ++kk)
+        if (!store_o(kk)) break;
+    // drain: every copy this warp issued has landed (and every O store has
+    // completed) before smem is released
     if (leader) {
+      if (is_k) bulk_wait_group0();
       int never = 0;
       for (int j = max(0, g - NS); j < g; ++j)
         mbar_wait_bounded(smem_u32(&full[j % NS]), (j / NS) & 1, &never, kTimeoutNs);
@@ -663,25 +697,33 @@ moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::kColO + c * 32), r + c * 32);
       tmem_ld_wait();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.o + ((int64_t)t_row * p.Hq + h_row) * D;
-      if (valid) {
-        // 32-byte stores where o allows them (half the store instructions of
-        // 16-byte ones: each store of the warp touches 32 rows)
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            v[i] = pack_bf16x2(__uint_as_float(r[16 * c + 2 * i]) * inv, __uint_as_float(r[16 * c + 2 * i + 1]) * inv);
-          if (p.o_v8) {
-            st_global_v8(orow + 16 * c, v);
-          } else {
-            reinterpret_cast<uint4*>(orow)[2 * c] = make_uint4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<uint4*>(orow)[2 * c + 1] = make_uint4(v[4], v[5], v[6], v[7]);
-          }
-        }
-        if (p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
+      // The row of o goes into the Q region (the next tile's Q is in TMEM by
+      // now) in the 128-byte-swizzled layout of the o tensor map's box, row
+      // `row` of each 64-column half; the K-producer thread writes the tile
+      // out with TMA stores, which skip the rows past T. The previous tile's
+      // store must have read the region first (it has whenever a next tile's
+      // Q was loaded into it; after the last tile it may still be reading).
+      if (k > 0 && !warp_wait(smem_u32(&bars->o_free), (k - 1) & 1, abort)) {
+        ok = false;
+        break;
       }
+      uint8_t* srow = smem + C::kOffQ + row * 128;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = pack_bf16x2(__uint_as_float(r[64 * c + 8 * i + 2 * e]) * inv,
+                               __uint_as_float(r[64 * c + 8 * i + 2 * e + 1]) * inv);
+          *reinterpret_cast<uint4*>(srow + c * C::kBoxBytes + ((i ^ (row & 7)) << 4)) =
+              make_uint4(v[0], v[1], v[2], v[3]);
+        }
+      // the TMA store reads these bytes through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&bars->o_staged));
+      if (valid && p.lse) p.lse[(int64_t)t_row * p.Hq + h_row] = m_ref * kLn2 + logf(l);
       // O has been read: the next tile's first P.V may overwrite it (that
       // P.V follows this warp's next p_full arrival, so program order suffices)
       tc_fence_before();
@@ -746,6 +788,13 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
     tkd = tk;  // never read when L == 0
     tvd = tv;
   }
+  CUtensorMap to;  // o [T][Hq][d]: the same boxes as q (a tile's rows, 64 columns each)
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.T};
+    const uint64_t str[2] = {row, row * a.Hq};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)P};
+    if (encode_bf16_sw128(&to, a.o, 3, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   Params prm;
   prm.T = a.T; prm.Hq = a.Hq; prm.Hk = a.Hk; prm.L = a.L; prm.lgG = lgG; prm.ntiles = ntiles;
   prm.depth_lm = a.layer_major;
@@ -753,8 +802,6 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   // K and V of every KV head, bf16: head-major order once they overflow half of L2
   prm.head_major = (uint64_t)a.Hk * a.T * D * 2 * 2 > (64ull << 20) ? 1 : 0;
   prm.scale_log2 = a.scale * kLog2e;
-  prm.o = (__nv_bfloat16*)a.o;
-  prm.o_v8 = ((uintptr_t)a.o & 31u) == 0;
   prm.lse = a.lse;
   prm.err = a.err;
   prm.queue = a.queue;
@@ -763,7 +810,8 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // one CTA per SM (each takes tiles from the queue until it is empty)
   const int grid = min(prm.total, a.num_sms > 0 ? a.num_sms : 148);
-  moda_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tkd, tvd, prm);
+  moda_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tkd, tvd, to,
+                                                                               prm);
   return cudaGetLastError();
 }
 
