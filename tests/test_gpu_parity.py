@@ -169,8 +169,9 @@ def test_lse_optional_and_status_clean():
 @pytest.mark.parametrize("d", [64, 128])
 def test_output_16_byte_aligned_only(d):
     """o at an address that is 16- but not 32-byte aligned (the ABI asks for
-    16): the rows go out in 16-byte stores, with the same values as from a
-    32-byte aligned o."""
+    16): the same values as at a 32-byte aligned o (d = 64 then writes its rows
+    in 16-byte stores; d = 128 writes through TMA stores, whose tensor map needs
+    only 16-byte alignment)."""
     w = Workload(f"o-align-d{d}", T=300, Hq=8, Hk=2, d=d, L=6, seed=31)
     x = {n: t.cuda() for n, t in make_inputs(w).items()}
     kd = moda.moda_pack_depth(x["kd"])
