@@ -570,8 +570,10 @@ cudaError_t launch_fwd_pp(const FwdArgs& a, cudaStream_t stream) {
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hk, (uint64_t)a.T, (uint64_t)a.L};
     const uint64_t str[3] = {row, row * a.Hk, row * a.Hk * a.T};
     const uint32_t box[4] = {64, 1, PW, 32 / PW};
-    if (encode_bf16_sw128(&tkd, a.kd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (encode_bf16_sw128(&tvd, a.vd, 4, dims, str, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // a depth row is 128 bytes here; the next 128 belong to another KV head,
+    // read by other CTAs at other times: fetch 128-byte granules
+    if (encode_bf16_sw128(&tkd, a.kd, 4, dims, str, box, 128) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_bf16_sw128(&tvd, a.vd, 4, dims, str, box, 128) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   } else if (a.L > 0) {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)a.Hk * a.T * a.L};
     const uint64_t str[1] = {row};

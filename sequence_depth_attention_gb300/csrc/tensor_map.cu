@@ -25,7 +25,8 @@ void resolve() {
 
 static CUresult encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides_bytes, const uint32_t* box,
-                            CUtensorMapSwizzle swizzle) {
+                            CUtensorMapSwizzle swizzle,
+                            CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   std::call_once(g_once, resolve);
   if (!g_encode) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t gdim[5];
@@ -39,12 +40,15 @@ static CUresult encode_bf16(CUtensorMap* m, const void* base, int rank, const ui
   for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_bytes[i];
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
                   gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  promotion, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 CUresult encode_bf16_sw128(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                           const uint64_t* strides_bytes, const uint32_t* box) {
-  return encode_bf16(m, base, rank, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_128B);
+                           const uint64_t* strides_bytes, const uint32_t* box,
+                           int l2_promotion_bytes) {
+  return encode_bf16(m, base, rank, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                     l2_promotion_bytes == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                               : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 CUresult encode_bf16_plain(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
