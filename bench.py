@@ -244,7 +244,8 @@ def config_of(w, n):
     kvd = 2 * w.L * w.T * w.Hk * w.d * 2
     return {"workload": w.name, "T": w.T, "Hq": w.Hq, "Hk": w.Hk, "G": w.G, "d": w.d, "L": w.L,
             "batch": 1, "causal": True, "scale": "1/sqrt(d)",
-            "step": "moda_pack_depth(kd) + moda_pack_depth(vd) + moda_fwd",
+            "step": "moda_fwd_layer_major on kd, vd [L,T,Hk,d] (the depth relayout happens in the "
+                    "forward's copies); the packed path is reported in packed_path",
             "l2": f"inputs larger than L2 (kd+vd {kvd / 1e9:.2f} GB, q {w.T * w.Hq * w.d * 2 / 1e6:.0f} MB)",
             "parallelism": f"replicas x{n}" if n > 1 else "single GPU"}
 
