@@ -50,12 +50,12 @@ bwd_delta_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __res
 // ---------------------------------------------------------------- 2. depth
 // Per-warp shared state; 16-byte aligned so that every warp's q/dO rows take
 // 16-byte accesses.
-template <int D, int G, bool LM>
+template <int D, int G, bool STAGE>
 struct alignas(16) DepthWarpSmem {
-  // layer-major only: the chunk's 32 kd and vd rows, 16-byte piece c of row r
+  // staged rows only: the chunk's 32 kd and vd rows, 16-byte piece c of row r
   // at c ^ (r % (D/8))
-  uint4 kr[LM ? 32 : 1][D / 8];
-  uint4 vr[LM ? 32 : 1][D / 8];
+  uint4 kr[STAGE ? 32 : 1][D / 8];
+  uint4 vr[STAGE ? 32 : 1][D / 8];
   __nv_bfloat16 qs[G][D];
   __nv_bfloat16 ds_[G][D];  // dO rows
   float P[G][32];
@@ -68,12 +68,15 @@ struct alignas(16) DepthWarpSmem {
 // slot and every head g of the group, p and ds (full-length dot products).
 // Phase 2: lanes split the d columns and walk the 32 slots of the chunk,
 // producing dvd and dkd rows (coalesced) and accumulating dq's depth share.
-// Packed depth (LM false): a position's slots are adjacent rows, and each
-// lane reads its own row straight from global memory. Layer-major (LM true):
-// the slots lie T*Hk rows apart, so the chunk's kd and vd rows are first
-// staged in shared memory with coalesced 16-byte loads, each lane then reading
-// its row in a swizzled order that puts the 32 lanes' rows in distinct banks.
-template <int D, int G, bool LM>
+// LM: depth layout, packed [Hk,T,L,d] (a position's slots are adjacent rows)
+// or layer-major [L,T,Hk,d] (the slots lie T*Hk rows apart). STAGE: the
+// chunk's kd and vd rows are first staged in shared memory with coalesced
+// 16-byte loads, each lane then reading its row in a swizzled order that puts
+// the 32 lanes' rows in distinct banks; without it each lane reads its own
+// row straight from global memory. Staging pays for layer-major rows and for
+// d = 64 rows (128 bytes); packed d = 128 rows keep the direct reads, where
+// the 16 KB of staging per warp costs more resident warps than it saves.
+template <int D, int G, bool LM, bool STAGE>
 __global__ void __launch_bounds__(128)
 bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kd,
                  const __nv_bfloat16* __restrict__ vd, const __nv_bfloat16* __restrict__ dO,
@@ -83,7 +86,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
   constexpr int E = D / 32;  // columns per lane in phase 2
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DepthWarpSmem<D, G, LM>& sm = reinterpret_cast<DepthWarpSmem<D, G, LM>*>(smem_raw)[warp];
+  DepthWarpSmem<D, G, STAGE>& sm = reinterpret_cast<DepthWarpSmem<D, G, STAGE>*>(smem_raw)[warp];
   const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
   if (pair >= (int64_t)Hk * T) return;
   const int hk = (int)(pair / T), t = (int)(pair - (int64_t)hk * T);
@@ -116,7 +119,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
   constexpr int CH = D / 8;  // 16-byte pieces per row
   for (int l0 = 0; l0 < L; l0 += 32) {
     const int nl = min(32, L - l0);
-    if constexpr (LM) {
+    if constexpr (STAGE) {
       // ---- stage the chunk's rows
 #pragma unroll 4
       for (int idx = lane; idx < 32 * CH; idx += 32) {
@@ -143,7 +146,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
         const uint4* vg = reinterpret_cast<const uint4*>(vd + (slot0 + l * lstride) * D);
         for (int ch = 0; ch < CH; ++ch) {
           uint4 kc, vc;
-          if constexpr (LM) {
+          if constexpr (STAGE) {
             kc = sm.kr[lane][ch ^ (lane & (CH - 1))];
             vc = sm.vr[lane][ch ^ (lane & (CH - 1))];
           } else {
@@ -185,7 +188,7 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
         // jj, at its swizzled place
         const int col = lane * E;
         const __nv_bfloat16* kr =
-            LM ? reinterpret_cast<const __nv_bfloat16*>(&sm.kr[jj][(col >> 3) ^ (jj & (CH - 1))]) +
+            STAGE ? reinterpret_cast<const __nv_bfloat16*>(&sm.kr[jj][(col >> 3) ^ (jj & (CH - 1))]) +
                      (col & 7)
                : kd + prow * D + col;
 #pragma unroll
@@ -234,14 +237,14 @@ bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __res
   }
 }
 
-template <int D, int G, bool LM>
+template <int D, int G, bool LM, bool STAGE>
 cudaError_t launch_depth_layout(const BwdArgs& a, cudaStream_t st) {
-  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G, LM>);
-  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G, LM>,
+  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G, STAGE>);
+  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G, LM, STAGE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs = (int64_t)a.Hk * a.T;
-  bwd_depth_kernel<D, G, LM><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
+  bwd_depth_kernel<D, G, LM, STAGE><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, (const __nv_bfloat16*)a.vd,
       (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.scale * kLog2e, a.scale,
       a.dq, a.dkd, a.dvd);
@@ -250,7 +253,9 @@ cudaError_t launch_depth_layout(const BwdArgs& a, cudaStream_t st) {
 
 template <int D, int G>
 cudaError_t launch_depth(const BwdArgs& a, cudaStream_t st) {
-  return a.layer_major ? launch_depth_layout<D, G, true>(a, st) : launch_depth_layout<D, G, false>(a, st);
+  if (a.layer_major) return launch_depth_layout<D, G, true, true>(a, st);
+  return D == 64 ? launch_depth_layout<D, G, false, true>(a, st)
+                 : launch_depth_layout<D, G, false, false>(a, st);
 }
 
 template <int D>
