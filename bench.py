@@ -19,8 +19,9 @@ Also reported on the same JSON line:
   packed_path     pack kd + pack vd + moda_fwd on the packed streams
   overhead_vs_L0  t_fwd(L) / t_fwd(L=0) - 1 for the same T, Hq, Hk, d
   roofline        the dominant kernel (the forward) against the measured peak
-  e2e             same metric with inputs copied from pinned host memory and
-                  o, lse copied back inside the timed region
+  e2e             same metric through the host-buffer call
+                  (moda_fwd_layer_major_host): inputs copied from pinned host
+                  memory and o, lse copied back inside the timed region
   cpu_baseline    the fp64 oracle on the host cores, on a bounded row sample
   clocks          nvidia-smi samples taken during the timed region
 """
@@ -533,75 +534,53 @@ def main(argv=None):
     if not args.no_e2e:
         hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hkd, hvd = (t.cpu().pin_memory() for t in (kd_raw, vd_raw))
-        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        # Double-buffered device inputs: the copy engines move step i+1's
-        # inputs (every byte of them, from pinned host memory) while step i
-        # runs on the compute stream; the host link is the bound.
-        copy = torch.cuda.Stream(device=dev)
-        sets = [(q, k, v, kd_raw, vd_raw)]
-        sets.append(tuple(torch.empty_like(t) for t in sets[0]))
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-        consumed = [torch.cuda.Event(), torch.cuda.Event()]
-        for ev in consumed:
-            ev.record(stream)
-        n_issued = [0]
+        # The library's host-buffer forward: each call copies that step's
+        # inputs (every byte of them, from pinned host memory) into a device
+        # workspace, runs the forward and copies o and lse back. Calls
+        # alternate between two streams, each with its own workspace and host
+        # outputs, so one call's copies overlap the other's forward; the host
+        # link is the bound.
+        streams2 = [stream, torch.cuda.Stream(device=dev)]
+        need = moda.moda_fwd_host_workspace_bytes(w.T, w.Hq, w.Hk, w.d, w.L)
+        wss = [torch.empty((need,), dtype=torch.uint8, device=dev) for _ in range(2)]
+        hos = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+        hls = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
 
-        def issue_copy(i):
-            dq, dk, dv, dkr, dvr = sets[i % 2]
-            copy.wait_event(consumed[i % 2])  # the set's previous step is done with it
-            with torch.cuda.stream(copy):
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk_, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                if w.L:
-                    dkr.copy_(hkd, non_blocking=True)
-                    dvr.copy_(hvd, non_blocking=True)
-                copied[i % 2].record(copy)
+        def e2e_step(i):
+            j = i % 2
+            moda.moda_fwd_layer_major_host(hq, hk_, hv, hkd if w.L else None,
+                                           hvd if w.L else None, w.scale, o=hos[j], lse=hls[j],
+                                           workspace=wss[j], stream=streams2[j])
 
-        def e2e_step(n):
-            """Step i of n: waits for its inputs, starts step i+1's copy (unless
-            it is the last), then runs the forward and reads back."""
-            i = n_issued[0]
-            n_issued[0] += 1
-            if i == 0:
-                issue_copy(0)
-            stream.wait_event(copied[i % 2])
-            if i + 1 < n:
-                issue_copy(i + 1)  # overlaps this step's compute
-            dq, dk, dv, dkr, dvr = sets[i % 2]
-            moda.moda_fwd_layer_major(dq, dk, dv, dkr if w.L else None, dvr if w.L else None,
-                                      w.scale, o=o, lse=lse, stream=stream)
-            consumed[i % 2].record(stream)
-            with torch.cuda.stream(stream):
-                ho.copy_(o, non_blocking=True)
-                hl.copy_(lse, non_blocking=True)
-
-        for _ in range(W):
-            e2e_step(W)
+        for i in range(W):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
-        n_issued[0] = 0
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(K):
-            e2e_step(K)
-        b.record(stream)
+        a.record(streams2[0])
+        streams2[1].wait_event(a)
+        for i in range(K):
+            e2e_step(i)
+        joined = torch.cuda.Event()
+        joined.record(streams2[1])
+        streams2[0].wait_event(joined)
+        b.record(streams2[0])
         barrier()
         e2e_ms = max_over_ranks(a.elapsed_time(b) / K, dist, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv)) + \
             (sum(t.numel() * t.element_size() for t in (hkd, hvd)) if w.L else 0)
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        d2h = hos[0].numel() * hos[0].element_size() + hls[0].numel() * hls[0].element_size()
         line["e2e"] = {"value": job_tflops(F, e2e_ms, world), "unit": "TFLOP/s",
                        "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h,
-                       "transfer": "every step's q, k, v, kd, vd copied from pinned host memory by "
-                                   "the copy engines into one of two device input sets, overlapping "
-                                   "the previous step's forward; o, lse copied back each step; "
-                                   "the timed region runs from the first step's copy to the last "
-                                   "step's read-back"}
+                       "transfer": "moda_fwd_layer_major_host every step: q, k, v, kd, vd copied "
+                                   "from pinned host memory into a device workspace, the forward, "
+                                   "o and lse copied back; calls alternate between two streams "
+                                   "and workspaces so one call's copies overlap the other's "
+                                   "forward; the timed region runs from the first call's first "
+                                   "copy to the last call's read-back"}
         host = {"q": hq, "k": hk_, "v": hv, "kd": hkd, "vd": hvd}
-        del sets  # the second device input set
+        del wss  # the two device workspaces
     else:
         host = None
 

@@ -256,6 +256,39 @@ MODA_API moda_status moda_fwd_layer_major(const void* q, const void* k, const vo
                                           float* lse, moda_stream_t stream);
 
 /*
+ * moda_fwd_layer_major_host -- moda_fwd_layer_major from and to HOST memory,
+ * for a caller whose tensors live on the host: the inputs are copied into the
+ * caller's device workspace, the forward runs there and o and lse are copied
+ * back, all enqueued on `stream` in that order (one cudaMemcpyAsync per
+ * tensor; the library allocates nothing).
+ *
+ *   q, k, v, kd, vd  host buffers with the shapes and layouts of
+ *                    moda_fwd_layer_major (kd, vd [L, T, Hk, d]; may be NULL
+ *                    when L == 0). Page-locked memory (cudaHostAlloc,
+ *                    cudaHostRegister) makes the copies asynchronous; pageable
+ *                    memory is accepted, its copies then go through the
+ *                    driver's staging buffers and the call may block until
+ *                    they are done
+ *   o, lse           host outputs ([T, Hq, d] bf16, [T, Hq] fp32; lse may be
+ *                    NULL), valid once the stream has passed the call
+ *   workspace        device memory owned by the caller, 256-byte aligned, at
+ *                    least moda_fwd_host_workspace_bytes(T, Hq, Hk, d, L)
+ *                    bytes: the device copies of every input and output
+ * The host inputs must stay unchanged, and the outputs unread, until the
+ * stream has passed the call; o and lse must not overlap each other or the
+ * workspace. Two calls on two streams with two workspaces overlap one call's
+ * copies with the other's forward.
+ * Errors: as moda_fwd; INVALID_ARG also for a NULL or too small workspace,
+ * MISALIGNED for a workspace that is not 256-byte aligned.
+ */
+MODA_API size_t moda_fwd_host_workspace_bytes(int T, int Hq, int Hk, int d, int L);
+MODA_API moda_status moda_fwd_layer_major_host(const void* q, const void* k, const void* v,
+                                               const void* kd, const void* vd, int T, int Hq,
+                                               int Hk, int d, int L, float scale, void* o,
+                                               float* lse, void* workspace,
+                                               size_t workspace_bytes, moda_stream_t stream);
+
+/*
  * moda_fwd_depth_cc -- the same result as moda_fwd, with the depth slots on
  * CUDA cores instead of tensor cores: the sequence part runs as moda_fwd with
  * L = 0, then one warp per (KV head, position) reads that position's L slots

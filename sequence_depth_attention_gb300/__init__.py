@@ -8,11 +8,15 @@ is an error; there is no CPU fallback.
 from .binding import (MODA_OK, ModaError, library_path, load, moda_bwd, moda_bwd_noalloc,
                       moda_decode, moda_decode_workspace_bytes, moda_depth_cache_admit,
                       moda_depth_mass, moda_depth_mass_workspace_bytes, moda_depth_write,
-                      moda_depth_write_at, moda_fwd, moda_fwd_layer_major, moda_get_device_error, moda_kv_proj_write,
-                      moda_pack_depth, moda_selftest_wait_timeout, moda_status_string)
+                      moda_depth_write_at, moda_fwd, moda_fwd_host_workspace_bytes,
+                      moda_fwd_layer_major, moda_fwd_layer_major_host, moda_get_device_error,
+                      moda_kv_proj_write, moda_pack_depth, moda_selftest_wait_timeout,
+                      moda_status_string)
 
 __all__ = ["MODA_OK", "ModaError", "library_path", "load", "moda_bwd", "moda_bwd_noalloc",
            "moda_decode", "moda_decode_workspace_bytes", "moda_depth_cache_admit",
            "moda_depth_mass", "moda_depth_mass_workspace_bytes", "moda_depth_write",
-           "moda_depth_write_at", "moda_fwd", "moda_fwd_layer_major", "moda_get_device_error", "moda_kv_proj_write",
-           "moda_pack_depth", "moda_selftest_wait_timeout", "moda_status_string"]
+           "moda_depth_write_at", "moda_fwd", "moda_fwd_host_workspace_bytes",
+           "moda_fwd_layer_major", "moda_fwd_layer_major_host", "moda_get_device_error",
+           "moda_kv_proj_write", "moda_pack_depth", "moda_selftest_wait_timeout",
+           "moda_status_string"]

@@ -26,7 +26,8 @@ _STATUS = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED",
 # every symbol include/moda.h declares
 EXPORTS = ("moda_pack_depth", "moda_depth_write", "moda_depth_write_at", "moda_depth_mass",
            "moda_depth_mass_workspace_bytes", "moda_depth_cache_admit", "moda_kv_proj_write",
-           "moda_fwd", "moda_fwd_layer_major", "moda_fwd_depth_cc", "moda_decode",
+           "moda_fwd", "moda_fwd_layer_major", "moda_fwd_layer_major_host",
+           "moda_fwd_host_workspace_bytes", "moda_fwd_depth_cc", "moda_decode",
            "moda_decode_strided",
            "moda_decode_workspace_bytes", "moda_bwd", "moda_bwd_layer_major", "moda_bwd_noalloc", "moda_get_device_error",
            "moda_selftest_wait_timeout", "moda_status_string", "moda_last_error_detail")
@@ -85,6 +86,11 @@ def load():
         lib.moda_fwd.restype = i
         lib.moda_fwd_layer_major.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, vp]
         lib.moda_fwd_layer_major.restype = i
+        lib.moda_fwd_host_workspace_bytes.argtypes = [i] * 5
+        lib.moda_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.moda_fwd_layer_major_host.argtypes = [vp] * 5 + [i] * 5 + [f, vp, vp, vp,
+                                                                        ctypes.c_size_t, vp]
+        lib.moda_fwd_layer_major_host.restype = i
         lib.moda_bwd.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
         lib.moda_bwd_layer_major.argtypes = [vp] * 8 + [i] * 5 + [f] + [vp] * 7
         lib.moda_bwd_layer_major.restype = i
@@ -319,6 +325,63 @@ def moda_fwd_layer_major(q, k, v, kd, vd, scale: float, o=None, lse=None, stream
     st = load().moda_fwd_layer_major(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk, d, L,
                                      float(scale), _ptr(o), _ptr(lse), _stream(stream))
     _check(st, "moda_fwd_layer_major")
+    return o, lse
+
+
+def moda_fwd_host_workspace_bytes(T: int, Hq: int, Hk: int, d: int, L: int) -> int:
+    return int(load().moda_fwd_host_workspace_bytes(int(T), int(Hq), int(Hk), int(d), int(L)))
+
+
+def _need_host(t, name, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name}: must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def moda_fwd_layer_major_host(q, k, v, kd, vd, scale: float, o=None, lse=None, workspace=None,
+                              device=None, stream=None, want_lse: bool = True):
+    """moda_fwd_layer_major from and to host memory: q, k, v, kd, vd are CPU
+    tensors (pinned for asynchronous copies; kd/vd [L,T,Hk,d] or None when
+    L == 0). The library copies them into `workspace` (a CUDA uint8 tensor of
+    at least moda_fwd_host_workspace_bytes bytes; allocated on `device` when
+    None), runs the forward there and copies o and lse back into host tensors
+    (allocated pinned when None), all on `stream`. Returns (o, lse); they are
+    valid once the stream has passed the call."""
+    _need_host(q, "q"), _need_host(k, "k"), _need_host(v, "v")
+    T, Hq, d = q.shape
+    Hk = k.shape[1]
+    if tuple(k.shape) != (T, Hk, d) or tuple(v.shape) != (T, Hk, d):
+        raise ValueError("k and v must be [T,Hk,d] matching q[T,Hq,d]")
+    if kd is None or kd.numel() == 0:
+        if kd is not None and kd.shape[0] != 0:
+            raise ValueError("empty kd with L > 0")
+        L, kd, vd = 0, None, None
+    else:
+        _need_host(kd, "kd"), _need_host(vd, "vd")
+        L = kd.shape[0]
+        if tuple(kd.shape) != (L, T, Hk, d) or tuple(vd.shape) != (L, T, Hk, d):
+            raise ValueError(f"kd/vd must be layer-major [L,T,Hk,d] = {(L, T, Hk, d)}")
+    if o is None:
+        o = torch.empty((T, Hq, d), dtype=torch.bfloat16, pin_memory=True)
+    _need_host(o, "o")
+    if want_lse and lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, pin_memory=True)
+    if lse is not None:
+        _need_host(lse, "lse", torch.float32)
+    need = moda_fwd_host_workspace_bytes(T, Hq, Hk, d, L)
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8)
+    st = load().moda_fwd_layer_major_host(_ptr(q), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd), T, Hq, Hk,
+                                          d, L, float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                                          workspace.numel(), _stream(stream))
+    _check(st, "moda_fwd_layer_major_host")
     return o, lse
 
 

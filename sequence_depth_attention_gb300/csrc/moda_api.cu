@@ -354,15 +354,12 @@ moda_status moda_kv_proj_write(const void* x, const void* wk, const void* wv, in
 }
 
 // Validation shared by the forward entry points; fills *out on success.
-static moda_status prepare_fwd(const void* q, const void* k, const void* v, const void* kd,
-                               const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
-                               void* o, float* lse, moda::FwdArgs* out, int layer_major = 0) {
-  if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL q, k, v or o");
+// The forward's shape and scale rules (everything but the pointers).
+static moda_status check_fwd_shape(int T, int Hq, int Hk, int d, int L, float scale) {
   if (T < 1) return fail(MODA_ERR_INVALID_ARG, "T = %d < 1", T);
   if (L < 0) return fail(MODA_ERR_INVALID_ARG, "L = %d < 0", L);
   if (Hk < 1 || Hq < 1) return fail(MODA_ERR_INVALID_ARG, "Hq = %d, Hk = %d", Hq, Hk);
   if (Hq % Hk != 0) return fail(MODA_ERR_INVALID_ARG, "Hq = %d not a multiple of Hk = %d", Hq, Hk);
-  if (L > 0 && (!kd || !vd)) return fail(MODA_ERR_INVALID_ARG, "NULL kd or vd with L = %d", L);
   if (!(scale > 0.f) || scale == __builtin_inff())
     return fail(MODA_ERR_INVALID_ARG, "scale must be positive and finite");
   const int G = Hq / Hk;
@@ -376,6 +373,17 @@ static moda_status prepare_fwd(const void* q, const void* k, const void* v, cons
   if ((int64_t)Hk * T * L + 128LL * L > 0x7fffffffLL)
     return fail(MODA_ERR_UNSUPPORTED, "Hk*T*L = %lld packed depth rows exceed 2^31 - 1 - 128*L",
                 (long long)Hk * T * L);
+  return MODA_OK;
+}
+
+static moda_status prepare_fwd(const void* q, const void* k, const void* v, const void* kd,
+                               const void* vd, int T, int Hq, int Hk, int d, int L, float scale,
+                               void* o, float* lse, moda::FwdArgs* out, int layer_major = 0) {
+  if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL q, k, v or o");
+  if (L > 0 && (!kd || !vd)) return fail(MODA_ERR_INVALID_ARG, "NULL kd or vd with L = %d", L);
+  moda_status sst = check_fwd_shape(T, Hq, Hk, d, L, scale);
+  if (sst != MODA_OK) return sst;
+  const int G = Hq / Hk;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (L > 0 && (!aligned16(kd) || !aligned16(vd))) || (lse && !aligned16(lse)))
     return fail(MODA_ERR_MISALIGNED, "a tensor pointer is not 16-byte aligned");
@@ -419,6 +427,86 @@ moda_status moda_fwd_layer_major(const void* q, const void* k, const void* v, co
   cudaError_t e = moda::launch_fwd_tc(a, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(MODA_ERR_CUDA, "moda_fwd_layer_major launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// Device workspace of moda_fwd_layer_major_host: the inputs, o and lse, each
+// region starting on a 256-byte boundary.
+namespace {
+struct HostFwdLayout {
+  size_t q, k, v, kd, vd, o, lse, total;
+};
+
+bool host_fwd_layout(int T, int Hq, int Hk, int d, int L, HostFwdLayout* h) {
+  if (T < 1 || Hq < 1 || Hk < 1 || d < 1 || L < 0) return false;
+  // reject sizes whose byte counts would not fit in 62 bits
+  const double big = (double)T * (double)(Hq > Hk ? Hq : Hk) * (double)d * (double)(L > 1 ? L : 1);
+  if (big > 4.0e17) return false;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t qb = (size_t)T * Hq * d * 2, kvb = (size_t)T * Hk * d * 2;
+  const size_t db = (size_t)L * T * Hk * d * 2, lb = (size_t)T * Hq * 4;
+  size_t off = 0;
+  h->q = off; off += up(qb);
+  h->k = off; off += up(kvb);
+  h->v = off; off += up(kvb);
+  h->kd = off; off += up(db);
+  h->vd = off; off += up(db);
+  h->o = off; off += up(qb);
+  h->lse = off; off += up(lb);
+  h->total = off;
+  return true;
+}
+}  // namespace
+
+size_t moda_fwd_host_workspace_bytes(int T, int Hq, int Hk, int d, int L) {
+  HostFwdLayout h;
+  return host_fwd_layout(T, Hq, Hk, d, L, &h) ? h.total : 0;
+}
+
+moda_status moda_fwd_layer_major_host(const void* q, const void* k, const void* v, const void* kd,
+                                      const void* vd, int T, int Hq, int Hk, int d, int L,
+                                      float scale, void* o, float* lse, void* workspace,
+                                      size_t workspace_bytes, moda_stream_t stream) {
+  if (!workspace) return fail(MODA_ERR_INVALID_ARG, "NULL workspace");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MODA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  moda_status st = check_fwd_shape(T, Hq, Hk, d, L, scale);
+  if (st != MODA_OK) return st;
+  HostFwdLayout h;
+  if (!host_fwd_layout(T, Hq, Hk, d, L, &h)) return fail(MODA_ERR_UNSUPPORTED, "tensor sizes overflow");
+  if (!q || !k || !v || !o) return fail(MODA_ERR_INVALID_ARG, "NULL host q, k, v or o");
+  if (L > 0 && (!kd || !vd)) return fail(MODA_ERR_INVALID_ARG, "NULL host kd or vd with L = %d", L);
+  if (workspace_bytes < h.total)
+    return fail(MODA_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, h.total);
+  const size_t qb = (size_t)T * Hq * d * 2, kvb = (size_t)T * Hk * d * 2;
+  const size_t db = (size_t)L * T * Hk * d * 2, lb = lse ? (size_t)T * Hq * 4 : 0;
+  if (overlaps(o, qb, lse, lb)) return fail(MODA_ERR_INVALID_ARG, "o and lse overlap");
+  const void* host[7] = {q, k, v, L ? kd : nullptr, L ? vd : nullptr, o, lse};
+  const size_t hostsz[7] = {qb, kvb, kvb, db, db, qb, lb};
+  for (int i = 0; i < 7; ++i)
+    if (overlaps(host[i], hostsz[i], workspace, h.total))
+      return fail(MODA_ERR_INVALID_ARG, "a host buffer overlaps the workspace");
+  // the device copies' placement in the workspace, and the device
+  moda::FwdArgs a;
+  st = prepare_fwd(ws + h.q, ws + h.k, ws + h.v, L ? ws + h.kd : nullptr,
+                               L ? ws + h.vd : nullptr, T, Hq, Hk, d, L, scale, ws + h.o,
+                               lse ? reinterpret_cast<float*>(ws + h.lse) : nullptr, &a, 1);
+  if (st != MODA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t dst[5] = {h.q, h.k, h.v, h.kd, h.vd};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+    if (hostsz[i]) e = cudaMemcpyAsync(ws + dst[i], host[i], hostsz[i], cudaMemcpyDefault, s);
+  if (e != cudaSuccess)
+    return fail(MODA_ERR_CUDA, "moda_fwd_layer_major_host input copy: %s", cudaGetErrorString(e));
+  e = moda::launch_fwd_tc(a, s);
+  if (e != cudaSuccess)
+    return fail(MODA_ERR_CUDA, "moda_fwd_layer_major_host launch: %s", cudaGetErrorString(e));
+  e = cudaMemcpyAsync(o, ws + h.o, qb, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && lse) e = cudaMemcpyAsync(lse, ws + h.lse, lb, cudaMemcpyDefault, s);
+  if (e != cudaSuccess)
+    return fail(MODA_ERR_CUDA, "moda_fwd_layer_major_host output copy: %s", cudaGetErrorString(e));
   return ok();
 }
 

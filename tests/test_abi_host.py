@@ -100,6 +100,48 @@ def test_fwd_layer_major_rejects(lib, kw, code):
     assert lib.moda_last_error_detail().decode() != ""
 
 
+WS = 0x80000000  # fake device workspace, 256-byte aligned
+
+
+def fwd_host(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.125, o=O,
+             lse=LSE, ws=WS, nbytes=None):
+    if nbytes is None:
+        nbytes = lib.moda_fwd_host_workspace_bytes(T, Hq, Hk, d, L)
+    return lib.moda_fwd_layer_major_host(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, ws,
+                                         nbytes, None)
+
+
+def test_fwd_host_workspace_bytes(lib):
+    # q 64 KB, k and v 32 KB, kd and vd 128 KB, o 64 KB, lse 2 KB, each region
+    # on a 256-byte boundary
+    assert lib.moda_fwd_host_workspace_bytes(128, 4, 2, 64, 4) == 460800
+    # 384-byte q, k, v and o each take two 256-byte units, kd and vd none
+    assert lib.moda_fwd_host_workspace_bytes(3, 1, 1, 64, 0) == 512 * 4 + 256
+    for bad in ((0, 4, 2, 64, 4), (128, 0, 2, 64, 4), (128, 4, 2, 64, -1)):
+        assert lib.moda_fwd_host_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), INVALID), (dict(ws=WS + 16), MISALIGNED), (dict(nbytes=460799), INVALID),
+    (dict(q=None), INVALID), (dict(o=None), INVALID), (dict(kd=None), INVALID),
+    (dict(T=0), INVALID), (dict(scale=float("nan")), INVALID), (dict(d=96), UNSUPPORTED),
+    (dict(Hq=6, Hk=2), UNSUPPORTED), (dict(L=1025), UNSUPPORTED),
+    (dict(lse=O + 1024), INVALID),             # lse inside o
+    (dict(o=WS + 4096), INVALID),              # a host buffer inside the workspace
+])
+def test_fwd_layer_major_host_rejects(lib, kw, code):
+    assert fwd_host(lib, **kw) == code
+    assert lib.moda_last_error_detail().decode() != ""
+
+
+def test_fwd_layer_major_host_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd_host(lib) == NO_DEVICE
+    assert fwd_host(lib, kd=None, vd=None, L=0, lse=None) == NO_DEVICE
+
+
 def fwd_cc(lib, q=A, k=B, v=C, kd=D, vd=E, T=128, Hq=4, Hk=2, d=64, L=4, scale=0.125, o=O, lse=LSE):
     return lib.moda_fwd_depth_cc(q, k, v, kd, vd, T, Hq, Hk, d, L, scale, o, lse, None)
 
