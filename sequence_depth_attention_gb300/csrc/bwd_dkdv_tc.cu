@@ -13,17 +13,19 @@
 // from the depth kernel. dk is written times the softmax scale.
 //
 // Roles (12 warps): warp 0 TMA (K, V once, then the Q/dO ring); warp 1 issues
-// MMAs; warps 4-7 and 8-11 each take 32 of the 64 columns for all 128 keys.
-// TMEM columns: two buffers b of S^T [128b,128b+64) and dP^T [128b+64,128b+128),
-// sub-tile c in buffer c&1; the elementwise warps write P^T|dS^T over the S^T
-// columns they read (per column half: 16 columns of P^T then 16 of dS^T, bf16
-// pairs); dV [256,256+d), dK [256+d,256+2d); for d = 64 also K [384,416) (bf16
-// pairs, copied once: the A operand of S^T, so those N = 64 MMAs read only the
-// Q sub-tile from shared memory).
-// Issue order: dP_0 S_0 dP_1 S_1, then per c: dV_c dK_c once P^T_c and dS^T_c
-// are stored, dP_{c+2} (its columns were free once the elementwise warps read
-// dP_c), and S_{c+2} once dV_c and dK_c have read buffer c&1. The tensor core
-// works on one sub-tile while the elementwise warps work on the next.
+// MMAs; warps 4-7 and 8-11 are the two elementwise warpgroups. At d = 128 each
+// group takes 32 of the 64 columns of every sub-tile; at d = 64 (where the
+// elementwise work per MMA flop doubles) the groups take alternate sub-tiles,
+// all 64 columns each, so two sub-tiles are worked on at once.
+// TMEM columns: B buffers b of S^T [128b,128b+64) and dP^T [128b+64,128b+128)
+// (B = 2 at d = 128, 3 at d = 64), sub-tile c in buffer c%B; the elementwise
+// warps write P^T|dS^T over the S^T columns they read (per column half: 16
+// columns of P^T then 16 of dS^T, bf16 pairs); dV [128B,128B+d) and dK
+// [128B+d,128B+2d), 512 columns in all.
+// Issue order: dP_c S_c for c < B, then per c: dV_c dK_c once P^T_c and dS^T_c
+// are stored, dP_{c+B} (its columns were free once the elementwise warps read
+// dP_c), and S_{c+B} once dV_c and dK_c have read buffer c%B. The tensor core
+// works on one sub-tile while the elementwise warps work on the next ones.
 // All waits are bounded; on expiry the CTA drains and latches MODA_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -54,21 +56,24 @@ struct KvCfg {
   static constexpr int kOffV = kOffK + kKTile;
   static constexpr int kOffQ = kOffV + kKTile;           // stage s: Q at kOffQ + s*2*kQTile
   static constexpr int kOffRow = kOffQ + kNS * 2 * kQTile;  // per-warp lse2 / D staging
-  static constexpr int kOffBar = kOffRow + 8 * 2 * 32 * 4;
+  // d = 64: the elementwise warpgroups take alternate sub-tiles (ping-pong)
+  static constexpr bool kPingPong = D == 64;
+  static constexpr int kHalves = kPingPong ? 2 : 1;  // column halves per thread and sub-tile
+  static constexpr int kB = D == 64 ? 3 : 2;         // S^T|dP^T buffers: 128*kB + 2*D = 512
+  static constexpr int kOffBar = kOffRow + 8 * kHalves * 64 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr bool kKInTmem = D == 64;  // with d = 128, dV and dK fill the rest of TMEM
-  static constexpr uint32_t kColS = 0, kColP = 64, kColBuf = 128, kColV = 256, kColK = 256 + D,
-                            kColKt = 256 + 2 * D;
+  static constexpr uint32_t kColS = 0, kColP = 64, kColBuf = 128, kColV = 128 * kB,
+                            kColK = 128 * kB + D;
+  static_assert(kColK + D == 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct alignas(8) KvBars {
   uint64_t kv_full;
   uint64_t q_full[6], q_empty[6];
-  uint64_t s_full[2];               // S^T, dP^T of buffer b computed
-  uint64_t pd_full[2], pd_done[2];  // P^T|dS^T of buffer b stored / consumed
-  uint64_t k_tmem;                  // the block's K rows are in TMEM (d = 64)
-  uint64_t mma_done;
+  uint64_t s_full[3];               // S^T, dP^T of buffer b computed
+  uint64_t pd_full[3], pd_done[3];  // P^T|dS^T of buffer b stored / consumed
+  uint64_t mma_done;                // every product of the CTA has completed
   uint32_t tmem_base;
   int abort;
 };
@@ -150,13 +155,12 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(smem_u32(&bars->q_full[s]), 1);
       mbar_init(smem_u32(&bars->q_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kB; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->pd_full[b]), 256);
+      mbar_init(smem_u32(&bars->pd_full[b]), C::kPingPong ? 128 : 256);
       mbar_init(smem_u32(&bars->pd_done[b]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
-    mbar_init(smem_u32(&bars->k_tmem), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -226,9 +230,9 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         return mbar_wait_bounded(smem_u32(bar), parity, abort, kTimeoutNs);
       };
       auto stage_of = [&](int i) { return (uint32_t)((i % C::kNS) * 2 * C::kQTile) >> 4; };
-      auto issue_dp = [&](int i) {  // dP^T_i = V dO_i^T into buffer i&1
+      auto issue_dp = [&](int i) {  // dP^T_i = V dO_i^T into buffer i%B
         const uint32_t qs = q_lo + stage_of(i) + (C::kQTile >> 4);
-        const uint32_t acc = tbase + (i & 1) * C::kColBuf + C::kColP;
+        const uint32_t acc = tbase + (i % C::kB) * C::kColBuf + C::kColP;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
@@ -236,22 +240,19 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           mma_ss(acc, desc_join(v_lo + ka, hi), desc_join(qs + qa, hi), idS, kk > 0);
         }
       };
-      auto issue_s = [&](int i) {  // S^T_i = K Q_i^T into buffer i&1; buffer i&1 is then complete
+      auto issue_s = [&](int i) {  // S^T_i = K Q_i^T into buffer i%B; buffer i%B is then complete
         const uint32_t qs = q_lo + stage_of(i);
-        const uint32_t acc = tbase + (i & 1) * C::kColBuf + C::kColS;
+        const uint32_t acc = tbase + (i % C::kB) * C::kColBuf + C::kColS;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = ((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4;
           const uint32_t qa = ((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4;
-          if constexpr (C::kKInTmem)
-            mma_ts(acc, tbase + C::kColKt + kk * 8, desc_join(qs + qa, hi), idS, kk > 0);
-          else
-            mma_ss(acc, desc_join(k_lo + ka, hi), desc_join(qs + qa, hi), idS, kk > 0);
+          mma_ss(acc, desc_join(k_lo + ka, hi), desc_join(qs + qa, hi), idS, kk > 0);
         }
-        tc_commit(smem_u32(&bars->s_full[i & 1]));
+        tc_commit(smem_u32(&bars->s_full[i % C::kB]));
       };
       auto issue_grad = [&](int i) {  // dV += P^T_i dO_i, dK += dS^T_i Q_i; frees stage and buffer
-        const int s = i % C::kNS, b = i & 1;
+        const int s = i % C::kNS, b = i % C::kB;
         const uint32_t qs = qmn_lo + stage_of(i);
         const uint32_t abuf = tbase + b * C::kColBuf + C::kColS;
         const uint32_t acc0 = i > 0 ? 1u : 0u;
@@ -265,8 +266,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_commit(smem_u32(&bars->q_empty[s]));
         tc_commit(smem_u32(&bars->pd_done[b]));
       };
-      bool ok = wait(&bars->kv_full, 0) && (!C::kKInTmem || wait(&bars->k_tmem, 0));
-      for (int i = 0; ok && i < n && i < 2; ++i) {
+      bool ok = wait(&bars->kv_full, 0);
+      for (int i = 0; ok && i < n && i < C::kB; ++i) {
         ok = wait(&bars->q_full[i], 0);
         if (ok) {
           tc_fence_after();
@@ -275,17 +276,18 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
       }
       for (int i = 0; ok && i < n; ++i) {
-        if (!wait(&bars->pd_full[i & 1], (i >> 1) & 1)) break;
+        if (!wait(&bars->pd_full[i % C::kB], (i / C::kB) & 1)) break;
         tc_fence_after();
         issue_grad(i);
-        if (i + 2 < n) {
-          if (!wait(&bars->q_full[(i + 2) % C::kNS], ((i + 2) / C::kNS) & 1)) break;
+        const int j = i + C::kB;
+        if (j < n) {
+          if (!wait(&bars->q_full[j % C::kNS], (j / C::kNS) & 1)) break;
           tc_fence_after();
-          issue_dp(i + 2);
-          // S^T_{i+2} overwrites the P^T|dS^T columns that dV_i and dK_i read
-          if (!wait(&bars->pd_done[i & 1], (i >> 1) & 1)) break;
+          issue_dp(j);
+          // S^T_j overwrites the P^T|dS^T columns that dV_i and dK_i read
+          if (!wait(&bars->pd_done[i % C::kB], (i / C::kB) & 1)) break;
           tc_fence_after();
-          issue_s(i + 2);
+          issue_s(j);
         }
       }
       int never = 0;
@@ -294,80 +296,65 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------------------------ P^T and dS^T (two column halves)
+    // ------------------------------------------------------ P^T and dS^T
     const int half = (warp - 4) >> 2, q4 = warp & 3;
     const int row = q4 * 32 + lane;  // key within the block
     const uint32_t lane_base = (uint32_t)q4 * 32;
     const int key = q0 + row;
-    // K row -> TMEM columns [kColKt, kColKt + d/2) as bf16 pairs in row order,
-    // the A operand of S^T = K Q^T for every sub-tile (so those MMAs read only
-    // the 64-row Q sub-tile from shared memory); the first half's warps copy it
-    if (C::kKInTmem && half == 0) {
-      bool kok = warp_wait(smem_u32(&bars->kv_full), 0, abort);
-      if (kok) {
-        const uint8_t* krow = smem + C::kOffK + row * 128;
-#pragma unroll
-        for (int c = 0; c < C::kBoxes; ++c) {
-          uint32_t w[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4*>(krow + c * C::kKBox + ((k ^ (row & 7)) << 4));
-            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-          }
-          tmem_st32(tmem_addr(tbase, lane_base, C::kColKt + c * 32), w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->k_tmem));
-      }
-    }
-    float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64;
+    // d = 128: group `half` takes column half `half` of every sub-tile; d = 64:
+    // group `half` takes sub-tiles half, half + 2, ..., both column halves
+    const int i0 = C::kPingPong ? half : 0, di = C::kPingPong ? 2 : 1;
+    const int h0 = C::kPingPong ? 0 : half;  // first column half of this thread
+    // per column half: -lse log2e of its 32 columns, then -D
+    float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64 * C::kHalves;
     const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
-    const int col = half * 32 + lane;  // the column this lane fetches lse and D for
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
+    for (int i = i0; i < n && ok; i += di) {
       const int t0 = q0 + i * PQ;
-      {
+      __syncwarp();  // the previous sub-tile's reads of rowbuf are done
+#pragma unroll
+      for (int hh = 0; hh < C::kHalves; ++hh) {
+        const int col = (h0 + hh) * 32 + lane;  // the column this lane fetches lse and D for
         const int t = t0 + (col >> p.lgG);
         const int64_t ri = (int64_t)t * p.Hq + hk * G + (col & (G - 1));
         const bool valid = t < p.T;
-        const float l2 = valid ? -__ldg(p.lse + ri) * kLog2e : -INFINITY;
-        const float dd = valid ? -__ldg(p.delta + ri) : 0.f;
-        __syncwarp();
-        rowbuf[lane] = l2;
-        rowbuf[32 + lane] = dd;
-        __syncwarp();
+        rowbuf[hh * 64 + lane] = valid ? -__ldg(p.lse + ri) * kLog2e : -INFINITY;
+        rowbuf[hh * 64 + 32 + lane] = valid ? -__ldg(p.delta + ri) : 0.f;
       }
-      const uint32_t buf = (i & 1) * C::kColBuf;
-      if (!warp_wait(smem_u32(&bars->s_full[i & 1]), (i >> 1) & 1, abort)) {
+      __syncwarp();
+      const uint32_t buf = (i % C::kB) * C::kColBuf;
+      if (!warp_wait(smem_u32(&bars->s_full[i % C::kB]), (i / C::kB) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t x[32], y[32];
-      tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColS + half * 32), x);
-      tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColP + half * 32), y);
-      tmem_ld_wait();
-      // causal: column c (position t0 + c/G) sees this key iff key <= position;
-      // sub-tiles at or after the block's last key need no mask
-      uint32_t pk[32];
-      if (t0 < q0 + BK - 1) {
-        const int first = (key - t0) * G - half * 32;  // first visible local column
-        pds_pack<true>(x, y, rowbuf, sl2, first, pk);
-      } else {
-        pds_pack<false>(x, y, rowbuf, sl2, 0, pk);
+#pragma unroll 1
+      for (int hh = 0; hh < C::kHalves; ++hh) {
+        const int h = h0 + hh;
+        uint32_t x[32], y[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColS + h * 32), x);
+        tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColP + h * 32), y);
+        tmem_ld_wait();
+        // causal: column c (position t0 + c/G) sees this key iff key <= position;
+        // sub-tiles at or after the block's last key need no mask
+        uint32_t pk[32];
+        if (t0 < q0 + BK - 1) {
+          const int first = (key - t0) * G - h * 32;  // first visible local column
+          pds_pack<true>(x, y, rowbuf + hh * 64, sl2, first, pk);
+        } else {
+          pds_pack<false>(x, y, rowbuf + hh * 64, sl2, 0, pk);
+        }
+        // in place over the S^T columns this thread has just read
+        tmem_st32(tmem_addr(tbase, lane_base, buf + C::kColS + h * 32), pk);
       }
-      // in place over the S^T columns this thread has just read
-      tmem_st32(tmem_addr(tbase, lane_base, buf + C::kColS + half * 32), pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->pd_full[i & 1]));
+      mbar_arrive(smem_u32(&bars->pd_full[i % C::kB]));
     }
-    if (ok) {
-      ok = warp_wait(smem_u32(&bars->pd_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, abort);
-      if (ok && n >= 2)
-        ok = warp_wait(smem_u32(&bars->pd_done[(n - 2) & 1]), ((n - 2) >> 1) & 1, abort);
-    }
+    // every product has completed once the issuer's final commit arrives (at
+    // d = 64 the other group may still be on its last sub-tile, so waiting on
+    // a pd_done phase here could look two uses ahead of the barrier)
+    if (ok) ok = warp_wait(smem_u32(&bars->mma_done), 0, abort);
     if (ok) {
       tc_fence_after();
       // half 0 writes dV, half 1 writes dK (times the softmax scale)
