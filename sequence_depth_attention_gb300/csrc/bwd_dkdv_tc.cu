@@ -13,10 +13,11 @@
 // from the depth kernel. dk is written times the softmax scale.
 //
 // Roles (12 warps): warp 0 TMA (K, V once, then the Q/dO ring); warp 1 issues
-// MMAs; warps 4-7 and 8-11 are the two elementwise warpgroups. At d = 128 each
-// group takes 32 of the 64 columns of every sub-tile; at d = 64 (where the
-// elementwise work per MMA flop doubles) the groups take alternate sub-tiles,
-// all 64 columns each, so two sub-tiles are worked on at once.
+// MMAs; warps 4-7 and 8-11 are the two elementwise warpgroups. Either each
+// group takes 32 of the 64 columns of every sub-tile, or (ping-pong: always at
+// d = 64, where the elementwise work per MMA flop doubles, and for long
+// sequences at d = 128) the groups take alternate sub-tiles, all 64 columns
+// each, so that two sub-tiles are worked on at once.
 // TMEM columns: B buffers b of S^T [128b,128b+64) and dP^T [128b+64,128b+128)
 // (B = 2 at d = 128, 3 at d = 64), sub-tile c in buffer c%B; the elementwise
 // warps write P^T|dS^T over the S^T columns they read (per column half: 16
@@ -56,11 +57,8 @@ struct KvCfg {
   static constexpr int kOffV = kOffK + kKTile;
   static constexpr int kOffQ = kOffV + kKTile;           // stage s: Q at kOffQ + s*2*kQTile
   static constexpr int kOffRow = kOffQ + kNS * 2 * kQTile;  // per-warp lse2 / D staging
-  // d = 64: the elementwise warpgroups take alternate sub-tiles (ping-pong)
-  static constexpr bool kPingPong = D == 64;
-  static constexpr int kHalves = kPingPong ? 2 : 1;  // column halves per thread and sub-tile
-  static constexpr int kB = D == 64 ? 3 : 2;         // S^T|dP^T buffers: 128*kB + 2*D = 512
-  static constexpr int kOffBar = kOffRow + 8 * kHalves * 64 * 4;
+  static constexpr int kB = D == 64 ? 3 : 2;  // S^T|dP^T buffers: 128*kB + 2*D = 512
+  static constexpr int kOffBar = kOffRow + 8 * 2 * 64 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr uint32_t kColS = 0, kColP = 64, kColBuf = 128, kColV = 128 * kB,
                             kColK = 128 * kB + D;
@@ -127,7 +125,8 @@ __device__ __forceinline__ void pds_pack(const uint32_t* x, const uint32_t* y, c
   }
 }
 
-template <int D>
+// PP: the elementwise warpgroups take alternate sub-tiles (ping-pong)
+template <int D, bool PP>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -147,6 +146,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int hk = (int)(blockIdx.x % p.Hk);
   const int q0 = kb * BK;                   // first query position that sees this block
   const int n = (p.T - q0 + PQ - 1) / PQ;   // sub-tiles
+  constexpr bool pp = PP;
 
   if (tid == 0) {
     bars->abort = 0;
@@ -157,7 +157,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     for (int b = 0; b < C::kB; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->pd_full[b]), C::kPingPong ? 128 : 256);
+      mbar_init(smem_u32(&bars->pd_full[b]), pp ? 128 : 256);
       mbar_init(smem_u32(&bars->pd_done[b]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
@@ -301,19 +301,20 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int row = q4 * 32 + lane;  // key within the block
     const uint32_t lane_base = (uint32_t)q4 * 32;
     const int key = q0 + row;
-    // d = 128: group `half` takes column half `half` of every sub-tile; d = 64:
-    // group `half` takes sub-tiles half, half + 2, ..., both column halves
-    const int i0 = C::kPingPong ? half : 0, di = C::kPingPong ? 2 : 1;
-    const int h0 = C::kPingPong ? 0 : half;  // first column half of this thread
+    // group `half` takes column half `half` of every sub-tile, or with
+    // ping-pong sub-tiles half, half + 2, ..., both column halves
+    constexpr int halves = pp ? 2 : 1;  // column halves per thread and sub-tile
+    const int i0 = pp ? half : 0, di = pp ? 2 : 1;
+    const int h0 = pp ? 0 : half;  // first column half of this thread
     // per column half: -lse log2e of its 32 columns, then -D
-    float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 64 * C::kHalves;
+    float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow) + (warp - 4) * 128;
     const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int i = i0; i < n && ok; i += di) {
       const int t0 = q0 + i * PQ;
       __syncwarp();  // the previous sub-tile's reads of rowbuf are done
 #pragma unroll
-      for (int hh = 0; hh < C::kHalves; ++hh) {
+      for (int hh = 0; hh < halves; ++hh) {
         const int col = (h0 + hh) * 32 + lane;  // the column this lane fetches lse and D for
         const int t = t0 + (col >> p.lgG);
         const int64_t ri = (int64_t)t * p.Hq + hk * G + (col & (G - 1));
@@ -329,7 +330,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int hh = 0; hh < C::kHalves; ++hh) {
+      for (int hh = 0; hh < halves; ++hh) {
         const int h = h0 + hh;
         uint32_t x[32], y[32];
         tmem_ld32(tmem_addr(tbase, lane_base, buf + C::kColS + h * 32), x);
@@ -351,9 +352,9 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->pd_full[i % C::kB]));
     }
-    // every product has completed once the issuer's final commit arrives (at
-    // d = 64 the other group may still be on its last sub-tile, so waiting on
-    // a pd_done phase here could look two uses ahead of the barrier)
+    // every product has completed once the issuer's final commit arrives
+    // (with ping-pong the other group may still be on its last sub-tile, so
+    // waiting on a pd_done phase here could look two uses ahead of the barrier)
     if (ok) ok = warp_wait(smem_u32(&bars->mma_done), 0, abort);
     if (ok) {
       tc_fence_after();
@@ -418,11 +419,16 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t stream) {
   prm.dk = a.dk;
   prm.dv = a.dv;
   prm.err = a.err;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // Ping-pong always at d = 64; at d = 128 it pays once blocks see thousands
+  // of sub-tiles (measured: 2-4 % faster at T = 32768 and 65536, 2-4 % slower
+  // at T <= 16384).
+  auto kern = bwd_dkdv_tc_kernel<D, true>;
+  if constexpr (D == 128) {
+    if (a.T < 32768) kern = bwd_dkdv_tc_kernel<D, false>;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_tc_kernel<D><<<(unsigned)((int64_t)nk * a.Hk), kThreads, C::kSmemBytes, stream>>>(
-      tq, to, tk, tv, prm);
+  kern<<<(unsigned)((int64_t)nk * a.Hk), kThreads, C::kSmemBytes, stream>>>(tq, to, tk, tv, prm);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,53 @@ def test_backward_large_sampled(w):
                 check(f"{w.name}.dvd[t={t},hk={hk}]", got[4][:, t, hk], dvd[sel].sum(0))
 
 
+@pytest.mark.parametrize("layer_major", [False, True], ids=["packed", "layer-major"])
+def test_backward_long_sequence_tail(layer_major):
+    """T >= 32768 at d = 128, where the dK/dV kernel's two elementwise
+    warpgroups take alternate sub-tiles: dk and dv of the last 1024 keys (key
+    blocks walking up to 32 sub-tiles, the ragged last one included), dq and
+    the depth gradients of sampled rows, against the oracle's row-subset
+    backward over every row that sees those keys."""
+    w = Workload("bwd-T32773-G2", T=32768 + 5, Hq=2, Hk=1, d=128, L=3, seed=15)
+    x = make_inputs(w, device="cuda")
+    dO = upstream(w)
+    q, k, v, dOg = x["q"], x["k"], x["v"], dO.cuda()
+    if layer_major:
+        kd, vd = x["kd"], x["vd"]
+        o, lse = moda.moda_fwd_layer_major(q, k, v, kd, vd, w.scale)
+    else:
+        kd, vd = moda.moda_pack_depth(x["kd"]), moda.moda_pack_depth(x["vd"])
+        o, lse = moda.moda_fwd(q, k, v, kd, vd, w.scale)
+    dq, dk, dv, dkd, dvd = moda.moda_bwd(q, k, v, kd, vd, o, lse, dOg, w.scale,
+                                         layer_major=layer_major)
+    torch.cuda.synchronize()
+    assert moda.moda_get_device_error() == 0
+    if not layer_major:  # packed [Hk,T,L,d] -> append layout [L,T,Hk,d]
+        dkd, dvd = dkd.permute(2, 1, 0, 3), dvd.permute(2, 1, 0, 3)
+    W = 1024
+    ts, _ = sample_rows(w.T, w.Hq, w.G, n_random=24)
+    ts = sorted(set(ts.tolist()) | set(range(w.T - W, w.T)))
+    rows = np.array([t * w.Hq + h for t in ts for h in range(w.Hq)])
+    tsel = torch.tensor(ts, device="cuda")
+    got_dq = dq.reshape(-1, w.d)[torch.from_numpy(rows).cuda()].cpu().numpy()
+    got_dk, got_dv = dk[w.T - W:].cpu().numpy(), dv[w.T - W:].cpu().numpy()
+    got_dkd, got_dvd = dkd[:, tsel].cpu().numpy(), dvd[:, tsel].cpu().numpy()  # [L, n, Hk, d]
+    b = {n: bf16_bits(t) for n, t in x.items()}
+    del x, dq, dk, dv, dkd, dvd
+    r_dq, r_dk, r_dv, r_dkd, r_dvd = oracle.default().backward_rows(
+        b["q"], b["k"], b["v"], b["kd"], b["vd"], bf16_bits(dO), w.scale, rows, w.T - W,
+        nthreads=gc.NTHREADS)
+    check("dq", got_dq, r_dq)
+    check("dk_tail", got_dk, r_dk)
+    check("dv_tail", got_dv, r_dv)
+    G = w.G
+    for i in range(len(ts)):
+        for hk in range(w.Hk):
+            sel = slice(i * w.Hq + hk * G, i * w.Hq + (hk + 1) * G)
+            check(f"dkd[t={ts[i]},hk={hk}]", got_dkd[:, i, hk], r_dkd[sel].sum(0))
+            check(f"dvd[t={ts[i]},hk={hk}]", got_dvd[:, i, hk], r_dvd[sel].sum(0))
+
+
 def test_backward_deterministic():
     w = Workload("bwd-det", T=500, Hq=8, Hk=2, d=128, L=12, seed=3)
     x = make_inputs(w)
