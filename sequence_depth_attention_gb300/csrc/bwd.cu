@@ -10,8 +10,8 @@
 // Four launches, every output row with one owner (no atomics):
 //   1. delta     D[t,h] = <dO[t,h], o[t,h]>                   (caller workspace)
 //   2. depth     one warp per (hk, t): the G rows x L slots of that position
-//                on CUDA cores -> dkd, dvd (in the layout of kd, vd: packed
-//                or layer-major) and dq's depth share, written as dq's
+//                on warp-level MMAs -> dkd, dvd (in the layout of kd, vd:
+//                packed or layer-major) and dq's depth share, written as dq's
 //                initial value
 //   3. dq        tcgen05 (bwd_dq_tc.cu), added to dq
 //   4. dk/dv     tcgen05 (bwd_dkdv_tc.cu)
@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 
 #include "moda_internal.h"
+#include "sm103.cuh"
+#include "warp_mma.cuh"
 
 namespace moda {
 namespace {
@@ -48,203 +50,227 @@ bwd_delta_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __res
 }
 
 // ---------------------------------------------------------------- 2. depth
-// Per-warp shared state; 16-byte aligned so that every warp's q/dO rows take
-// 16-byte accesses.
-template <int D, int G, bool STAGE>
+// One warp per (KV head hk, position t): the G query rows of the pair against
+// the L depth slots of t, 32 slots per chunk, on warp-level tensor-core MMAs
+// (mma.sync m16n8k16, bf16 operands, fp32 accumulation; the G rows are rows
+// 0..G-1 of the 16-row A tiles, the rest zero):
+//   S = Q Kd^T, dP = dO Vd^T                          (16 x 32 per chunk)
+//   P = exp2(S scale log2e - lse log2e), dS = P (dP - D)   (in registers)
+//   dvd = P^T dO, dkd = scale dS^T Q                  (32 x d per chunk, stored)
+//   dq = scale dS Kd                                  (16 x d, over all chunks)
+// P and dS are rounded to bf16 as MMA operands, as in the sequence kernels.
+// LM: depth layout, packed [Hk,T,L,d] (a position's slots are adjacent rows)
+// or layer-major [L,T,Hk,d] (the slots lie T*Hk rows apart); each chunk's kd
+// and vd rows are copied to shared memory by 16-byte cp.async, piece c of row
+// r at c ^ (r % (D/8)) so that the ldmatrix row reads hit distinct banks.
+template <int D, int G>
 struct alignas(16) DepthWarpSmem {
-  // staged rows only: the chunk's 32 kd and vd rows, 16-byte piece c of row r
-  // at c ^ (r % (D/8))
-  uint4 kr[STAGE ? 32 : 1][D / 8];
-  uint4 vr[STAGE ? 32 : 1][D / 8];
-  __nv_bfloat16 qs[G][D];
-  __nv_bfloat16 ds_[G][D];  // dO rows
-  float P[G][32];
-  float S[G][32];           // ds values
-  float lse2[G];
-  float Dd[G];
+  static constexpr int R = G < 8 ? 8 : G;  // q/dO rows held (rows >= G are zero)
+  static constexpr int QS = D + 8;         // padded q/dO row: ldmatrix rows in distinct banks
+  uint4 kr[32][D / 8];
+  uint4 vr[32][D / 8];
+  __nv_bfloat16 qs[R][QS];
+  __nv_bfloat16 os[R][QS];  // dO rows
 };
 
-// One warp per (hk, t), 32 slots at a time. Phase 1: lane l computes, for its
-// slot and every head g of the group, p and ds (full-length dot products).
-// Phase 2: lanes split the d columns and walk the 32 slots of the chunk,
-// producing dvd and dkd rows (coalesced) and accumulating dq's depth share.
-// LM: depth layout, packed [Hk,T,L,d] (a position's slots are adjacent rows)
-// or layer-major [L,T,Hk,d] (the slots lie T*Hk rows apart). STAGE: the
-// chunk's kd and vd rows are first staged in shared memory with coalesced
-// 16-byte loads, each lane then reading its row in a swizzled order that puts
-// the 32 lanes' rows in distinct banks; without it each lane reads its own
-// row straight from global memory. Staging pays for layer-major rows and for
-// d = 64 rows (128 bytes); packed d = 128 rows keep the direct reads, where
-// the 16 KB of staging per warp costs more resident warps than it saves.
-template <int D, int G, bool LM, bool STAGE>
+template <int D, int G, bool LM>
 __global__ void __launch_bounds__(128)
 bwd_depth_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kd,
                  const __nv_bfloat16* __restrict__ vd, const __nv_bfloat16* __restrict__ dO,
                  const float* __restrict__ lse, const float* __restrict__ delta, int T, int Hq,
                  int Hk, int L, float scale_log2, float scale, float* __restrict__ dq,
                  float* __restrict__ dkd, float* __restrict__ dvd) {
-  constexpr int E = D / 32;  // columns per lane in phase 2
+  using W = DepthWarpSmem<D, G>;
+  using namespace wmma16;
+  constexpr int CH = D / 8;    // 16-byte pieces per row
+  constexpr int NT = D / 8;    // 8-column tiles of a d-wide row
+  constexpr bool kHi = G > 8;  // rows 8..15 of the A tiles hold query heads
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DepthWarpSmem<D, G, STAGE>& sm = reinterpret_cast<DepthWarpSmem<D, G, STAGE>*>(smem_raw)[warp];
+  W& sm = reinterpret_cast<W*>(smem_raw)[warp];
   const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
   if (pair >= (int64_t)Hk * T) return;
   const int hk = (int)(pair / T), t = (int)(pair - (int64_t)hk * T);
   const int64_t row0 = (int64_t)t * Hq + hk * G;  // row of head g is row0 + g
 
-  // stage q and dO rows of the group (16-byte chunks)
-  for (int idx = lane; idx < G * D / 8; idx += 32) {
-    const int g = idx / (D / 8), ch = idx % (D / 8);
-    reinterpret_cast<uint4*>(&sm.qs[g][0])[ch] =
-        reinterpret_cast<const uint4*>(q + (row0 + g) * D)[ch];
-    reinterpret_cast<uint4*>(&sm.ds_[g][0])[ch] =
-        reinterpret_cast<const uint4*>(dO + (row0 + g) * D)[ch];
+  // q and dO rows of the group; rows G..R-1 zero
+  for (int idx = lane; idx < W::R * CH; idx += 32) {
+    const int g = idx / CH, ch = idx % CH;
+    uint4 qv = make_uint4(0u, 0u, 0u, 0u), ov = qv;
+    if (g < G) {
+      qv = __ldg(reinterpret_cast<const uint4*>(q + (row0 + g) * D) + ch);
+      ov = __ldg(reinterpret_cast<const uint4*>(dO + (row0 + g) * D) + ch);
+    }
+    *reinterpret_cast<uint4*>(&sm.qs[g][ch * 8]) = qv;
+    *reinterpret_cast<uint4*>(&sm.os[g][ch * 8]) = ov;
   }
-  if (lane < G) {
-    sm.lse2[lane] = lse[row0 + lane] * kLog2e;
-    sm.Dd[lane] = delta[row0 + lane];
-  }
-  __syncwarp();
+  // this thread's rows of the accumulator fragments: g_lo and g_lo + 8
+  const int g_lo = lane >> 2;
+  const float lse_lo = g_lo < G ? __ldg(lse + row0 + g_lo) * kLog2e : 0.f;
+  const float d_lo = g_lo < G ? __ldg(delta + row0 + g_lo) : 0.f;
+  const float lse_hi = kHi ? __ldg(lse + row0 + g_lo + 8) * kLog2e : 0.f;
+  const float d_hi = kHi ? __ldg(delta + row0 + g_lo + 8) : 0.f;
 
-  float dqa[G][E];
+  float dqa[NT][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < E; ++e) dqa[g][e] = 0.f;
+  for (int c = 0; c < NT; ++c) dqa[c][0] = dqa[c][1] = dqa[c][2] = dqa[c][3] = 0.f;
 
   // row (of D values) of slot l: slot0 + l * lstride, in kd/vd and in dkd/dvd
   // alike; packed [Hk, T, L, d] or layer-major [L, T, Hk, d]
   const int64_t slot0 = LM ? (int64_t)t * Hk + hk : ((int64_t)hk * T + t) * L;
   const int64_t lstride = LM ? (int64_t)T * Hk : 1;
-  constexpr int CH = D / 8;  // 16-byte pieces per row
+  const uint32_t kr0 = sm103::smem_u32(&sm.kr[0][0]), vr0 = sm103::smem_u32(&sm.vr[0][0]);
+  const uint32_t qs0 = sm103::smem_u32(&sm.qs[0][0]), os0 = sm103::smem_u32(&sm.os[0][0]);
+  // byte offset of 16-byte piece c of staged row r
+  auto piece = [](int r, int c) -> uint32_t { return (uint32_t)((r * CH + (c ^ (r & (CH - 1)))) * 16); };
+  const int lr = lane & 7, lm = lane >> 3;  // ldmatrix: the row this lane addresses, its matrix
+
   for (int l0 = 0; l0 < L; l0 += 32) {
     const int nl = min(32, L - l0);
-    if constexpr (STAGE) {
-      // ---- stage the chunk's rows
+    __syncwarp();  // the previous chunk's reads of the staged rows are done
 #pragma unroll 4
-      for (int idx = lane; idx < 32 * CH; idx += 32) {
-        const int r = idx / CH, c = idx % CH;
-        uint4 kc = make_uint4(0u, 0u, 0u, 0u), vc = kc;
-        if (r < nl) {
-          const int64_t row = slot0 + (int64_t)(l0 + r) * lstride;
-          kc = __ldg(reinterpret_cast<const uint4*>(kd + row * D) + c);
-          vc = __ldg(reinterpret_cast<const uint4*>(vd + row * D) + c);
-        }
-        sm.kr[r][c ^ (r & (CH - 1))] = kc;
-        sm.vr[r][c ^ (r & (CH - 1))] = vc;
-      }
-      __syncwarp();
+    for (int idx = lane; idx < 32 * CH; idx += 32) {
+      const int r = idx / CH, c = idx % CH;
+      const bool ok = r < nl;
+      const int64_t row = slot0 + (int64_t)(l0 + (ok ? r : 0)) * lstride;
+      cp_async16(kr0 + piece(r, c), kd + row * D + c * 8, ok ? 16u : 0u);
+      cp_async16(vr0 + piece(r, c), vd + row * D + c * 8, ok ? 16u : 0u);
     }
-    // ---- phase 1: lane owns slot l0 + lane
-    {
-      const int l = l0 + lane;
-      float s[G], dp[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] = dp[g] = 0.f;
-      if (l < L) {
-        const uint4* kg = reinterpret_cast<const uint4*>(kd + (slot0 + l * lstride) * D);
-        const uint4* vg = reinterpret_cast<const uint4*>(vd + (slot0 + l * lstride) * D);
-        for (int ch = 0; ch < CH; ++ch) {
-          uint4 kc, vc;
-          if constexpr (STAGE) {
-            kc = sm.kr[lane][ch ^ (lane & (CH - 1))];
-            vc = sm.vr[lane][ch ^ (lane & (CH - 1))];
-          } else {
-            kc = __ldg(kg + ch);
-            vc = __ldg(vg + ch);
-          }
-          const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kc);
-          const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vc);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const uint4 qc = reinterpret_cast<const uint4*>(&sm.qs[g][0])[ch];
-            const uint4 oc = reinterpret_cast<const uint4*>(&sm.ds_[g][0])[ch];
-            const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qc);
-            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&oc);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 a = __bfloat1622float2(q2[i]), b = __bfloat1622float2(k2[i]);
-              const float2 c = __bfloat1622float2(o2[i]), dd = __bfloat1622float2(v2[i]);
-              s[g] = fmaf(a.x, b.x, fmaf(a.y, b.y, s[g]));
-              dp[g] = fmaf(c.x, dd.x, fmaf(c.y, dd.y, dp[g]));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float p = l < L ? exp2f(s[g] * scale_log2 - sm.lse2[g]) : 0.f;
-        sm.P[g][lane] = p;
-        sm.S[g][lane] = p * (dp[g] - sm.Dd[g]);
-      }
-    }
+    cp_async_wait_all();
     __syncwarp();
-    // ---- phase 2: lane owns columns lane*E .. lane*E+E-1
-    for (int jj = 0; jj < nl; ++jj) {
-      const int64_t prow = slot0 + (l0 + jj) * lstride;
-      float kdv[E];
+
+    // ---- S = Q Kd^T, dP = dO Vd^T: n-tile nt holds slots 8nt..8nt+7
+    float sc[4][4], dpc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[nt][i] = dpc[nt][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t aq[4], ao[4];
+      if constexpr (kHi) {
+        // matrices: rows 0-7 | rows 8-15, columns 16ks.. | 16ks+8..
+        const uint32_t off = (uint32_t)(((lm & 1) * 8 + lr) * W::QS + ks * 16 + (lm >> 1) * 8) * 2;
+        ldsm_x4(qs0 + off, aq[0], aq[1], aq[2], aq[3]);
+        ldsm_x4(os0 + off, ao[0], ao[1], ao[2], ao[3]);
+      } else {
+        const uint32_t off = (uint32_t)(lr * W::QS + ks * 16 + (lm & 1) * 8) * 2;
+        ldsm_x2(qs0 + off, aq[0], aq[2]);
+        ldsm_x2(os0 + off, ao[0], ao[2]);
+        aq[1] = aq[3] = ao[1] = ao[3] = 0u;
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        // matrices: kd pieces 2ks, 2ks+1, vd pieces 2ks, 2ks+1 of slots 8nt..8nt+7
+        const int r = nt * 8 + lr;
+        const uint32_t base = (lm < 2 ? kr0 : vr0) + piece(r, 2 * ks + (lm & 1));
+        uint32_t bk0, bk1, bv0, bv1;
+        ldsm_x4(base, bk0, bk1, bv0, bv1);
+        mma_bf16(sc[nt], aq, bk0, bk1);
+        mma_bf16(dpc[nt], ao, bv0, bv1);
+      }
+    }
+    // ---- P and dS as bf16 pairs: [nt][0] row g_lo, [nt][1] row g_lo + 8,
+    // slots 8nt + 2(lane%4) and +1; zero for rows >= G and slots >= nl
+    uint32_t pa[4][2], da[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int sl = nt * 8 + 2 * (lane & 3);
+      const bool v0 = sl < nl, v1 = sl + 1 < nl;
       {
-        // layer-major: columns lane*E.. lie in piece (lane*E)/8 of staged row
-        // jj, at its swizzled place
-        const int col = lane * E;
-        const __nv_bfloat16* kr =
-            STAGE ? reinterpret_cast<const __nv_bfloat16*>(&sm.kr[jj][(col >> 3) ^ (jj & (CH - 1))]) +
-                     (col & 7)
-               : kd + prow * D + col;
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kr + e));
-          kdv[e] = f.x;
-          kdv[e + 1] = f.y;
-        }
+        const bool row_ok = g_lo < G;
+        const float p0 = row_ok && v0 ? exp2f(sc[nt][0] * scale_log2 - lse_lo) : 0.f;
+        const float p1 = row_ok && v1 ? exp2f(sc[nt][1] * scale_log2 - lse_lo) : 0.f;
+        pa[nt][0] = pack_bf16(p0, p1);
+        da[nt][0] = pack_bf16(p0 * (dpc[nt][0] - d_lo), p1 * (dpc[nt][1] - d_lo));
       }
-      float dvv[E], dkv[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) dvv[e] = dkv[e] = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pg = sm.P[g][jj], dsg = sm.S[g][jj];
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 qq = __bfloat1622float2(
-              *reinterpret_cast<const __nv_bfloat162*>(&sm.qs[g][lane * E + e]));
-          const float2 oo = __bfloat1622float2(
-              *reinterpret_cast<const __nv_bfloat162*>(&sm.ds_[g][lane * E + e]));
-          dvv[e] = fmaf(pg, oo.x, dvv[e]);
-          dvv[e + 1] = fmaf(pg, oo.y, dvv[e + 1]);
-          dkv[e] = fmaf(dsg, qq.x, dkv[e]);
-          dkv[e + 1] = fmaf(dsg, qq.y, dkv[e + 1]);
-          dqa[g][e] = fmaf(dsg, kdv[e], dqa[g][e]);
-          dqa[g][e + 1] = fmaf(dsg, kdv[e + 1], dqa[g][e + 1]);
-        }
-      }
-      float* dvo = dvd + prow * D + lane * E;
-      float* dko = dkd + prow * D + lane * E;
-#pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        *reinterpret_cast<float2*>(dvo + e) = make_float2(dvv[e], dvv[e + 1]);
-        *reinterpret_cast<float2*>(dko + e) = make_float2(dkv[e] * scale, dkv[e + 1] * scale);
+      if constexpr (kHi) {
+        const float p0 = v0 ? exp2f(sc[nt][2] * scale_log2 - lse_hi) : 0.f;
+        const float p1 = v1 ? exp2f(sc[nt][3] * scale_log2 - lse_hi) : 0.f;
+        pa[nt][1] = pack_bf16(p0, p1);
+        da[nt][1] = pack_bf16(p0 * (dpc[nt][2] - d_hi), p1 * (dpc[nt][3] - d_hi));
+      } else {
+        pa[nt][1] = da[nt][1] = 0u;
       }
     }
-    __syncwarp();
+    // ---- dq += dS Kd: k-step kk covers slots 16kk..16kk+15; B = Kd read
+    // transposed (k = slot, n = column)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t a[4] = {da[2 * kk][0], da[2 * kk][1], da[2 * kk + 1][0], da[2 * kk + 1][1]};
+#pragma unroll
+      for (int ct = 0; ct < NT; ct += 2) {
+        // matrices: slots 16kk..+7 | 16kk+8..+15, columns 8ct.. | 8ct+8..
+        const int r = 16 * kk + (lm & 1) * 8 + lr;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(kr0 + piece(r, ct + (lm >> 1)), b0, b1, b2, b3);
+        mma_bf16(dqa[ct], a, b0, b1);
+        mma_bf16(dqa[ct + 1], a, b2, b3);
+      }
+    }
+    // ---- dvd = P^T dO, dkd = scale dS^T Q: m-tile mt covers slots
+    // 16mt..16mt+15 (A = the transposed P / dS blocks), B = dO / Q read
+    // transposed (k = row g, n = column)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const uint32_t ap[4] = {movmatrix_t(pa[2 * mt][0]), movmatrix_t(pa[2 * mt + 1][0]),
+                              kHi ? movmatrix_t(pa[2 * mt][1]) : 0u,
+                              kHi ? movmatrix_t(pa[2 * mt + 1][1]) : 0u};
+      const uint32_t ad[4] = {movmatrix_t(da[2 * mt][0]), movmatrix_t(da[2 * mt + 1][0]),
+                              kHi ? movmatrix_t(da[2 * mt][1]) : 0u,
+                              kHi ? movmatrix_t(da[2 * mt + 1][1]) : 0u};
+      const int s_lo = 16 * mt + g_lo, s_hi = s_lo + 8;  // chunk-local slots of this thread's rows
+      float* dv_lo = dvd + (slot0 + (int64_t)(l0 + s_lo) * lstride) * D + 2 * (lane & 3);
+      float* dk_lo = dkd + (slot0 + (int64_t)(l0 + s_lo) * lstride) * D + 2 * (lane & 3);
+      float* dv_hi = dvd + (slot0 + (int64_t)(l0 + s_hi) * lstride) * D + 2 * (lane & 3);
+      float* dk_hi = dkd + (slot0 + (int64_t)(l0 + s_hi) * lstride) * D + 2 * (lane & 3);
+#pragma unroll
+      for (int ct = 0; ct < NT; ++ct) {
+        uint32_t bo0, bo1, bq0, bq1;
+        if constexpr (kHi) {
+          // matrices: dO rows 0-7, 8-15, Q rows 0-7, 8-15 at columns 8ct..
+          const uint32_t off = (uint32_t)(((lm & 1) * 8 + lr) * W::QS + ct * 8) * 2;
+          ldsm_x4_t((lm < 2 ? os0 : qs0) + off, bo0, bo1, bq0, bq1);
+        } else {
+          const uint32_t off = (uint32_t)(lr * W::QS + ct * 8) * 2;
+          ldsm_x2_t((lm & 1 ? qs0 : os0) + off, bo0, bq0);
+          bo1 = bq1 = 0u;
+        }
+        float cv[4] = {0.f, 0.f, 0.f, 0.f}, ck[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(cv, ap, bo0, bo1);
+        mma_bf16(ck, ad, bq0, bq1);
+        if (s_lo < nl) {
+          *reinterpret_cast<float2*>(dv_lo + ct * 8) = make_float2(cv[0], cv[1]);
+          *reinterpret_cast<float2*>(dk_lo + ct * 8) = make_float2(ck[0] * scale, ck[1] * scale);
+        }
+        if (s_hi < nl) {
+          *reinterpret_cast<float2*>(dv_hi + ct * 8) = make_float2(cv[2], cv[3]);
+          *reinterpret_cast<float2*>(dk_hi + ct * 8) = make_float2(ck[2] * scale, ck[3] * scale);
+        }
+      }
+    }
   }
+  // dq's depth share (its initial value; the sequence share is added later)
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float* out = dq + (row0 + g) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; e += 2)
-      *reinterpret_cast<float2*>(out + e) = make_float2(dqa[g][e] * scale, dqa[g][e + 1] * scale);
+  for (int ct = 0; ct < NT; ++ct) {
+    const int col = ct * 8 + 2 * (lane & 3);
+    if (g_lo < G)
+      *reinterpret_cast<float2*>(dq + (row0 + g_lo) * D + col) =
+          make_float2(dqa[ct][0] * scale, dqa[ct][1] * scale);
+    if (kHi)
+      *reinterpret_cast<float2*>(dq + (row0 + g_lo + 8) * D + col) =
+          make_float2(dqa[ct][2] * scale, dqa[ct][3] * scale);
   }
 }
 
-template <int D, int G, bool LM, bool STAGE>
+template <int D, int G, bool LM>
 cudaError_t launch_depth_layout(const BwdArgs& a, cudaStream_t st) {
-  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G, STAGE>);
-  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G, LM, STAGE>,
+  const size_t smem = 4 * sizeof(DepthWarpSmem<D, G>);
+  cudaError_t e = cudaFuncSetAttribute(bwd_depth_kernel<D, G, LM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs = (int64_t)a.Hk * a.T;
-  bwd_depth_kernel<D, G, LM, STAGE><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
+  bwd_depth_kernel<D, G, LM><<<(unsigned)((pairs + 3) / 4), 128, smem, st>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, (const __nv_bfloat16*)a.vd,
       (const __nv_bfloat16*)a.dO, a.lse, a.delta, a.T, a.Hq, a.Hk, a.L, a.scale * kLog2e, a.scale,
       a.dq, a.dkd, a.dvd);
@@ -253,9 +279,7 @@ cudaError_t launch_depth_layout(const BwdArgs& a, cudaStream_t st) {
 
 template <int D, int G>
 cudaError_t launch_depth(const BwdArgs& a, cudaStream_t st) {
-  if (a.layer_major) return launch_depth_layout<D, G, true, true>(a, st);
-  return D == 64 ? launch_depth_layout<D, G, false, true>(a, st)
-                 : launch_depth_layout<D, G, false, false>(a, st);
+  return a.layer_major ? launch_depth_layout<D, G, true>(a, st) : launch_depth_layout<D, G, false>(a, st);
 }
 
 template <int D>

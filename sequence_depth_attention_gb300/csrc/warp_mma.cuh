@@ -1,5 +1,6 @@
-// Warp-level MMA helpers (mma.sync m16n8k16 bf16 -> fp32, ldmatrix) used by
-// the decode kernel, whose per-token work is too small for tcgen05 tiles.
+// Warp-level MMA helpers (mma.sync m16n8k16 bf16 -> fp32, ldmatrix, movmatrix,
+// 16-byte cp.async) used by the decode kernel and the backward's depth kernel,
+// whose per-token and per-position work is too small for tcgen05 tiles.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -15,6 +16,30 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a, uint32_t& b,
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(a), "=r"(b) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(a), "=r"(b) : "r"(addr));
+}
+// The transpose of an 8x8 b16 matrix held in the fragment layout (thread i:
+// row i/4, columns 2(i%4) and 2(i%4)+1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
+}
+// 16-byte global -> shared copy; src_bytes 0 fills the destination with zeros
+// (the source is then not read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
