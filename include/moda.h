@@ -20,8 +20,8 @@
  *     moda_get_device_error().
  *   - Batch is 1; callers loop over sequences.
  *   - Thread safety: calls may be made from several host threads.
- *   - moda_fwd and moda_fwd_layer_major at d = 128 hand out their tiles
- *     through a small per-device queue; each call takes the next of 64 queues
+ *   - moda_fwd, moda_fwd_layer_major and moda_fwd_depth_cc hand out their
+ *     tiles through a small per-device queue; each call takes the next of 64 queues
  *     in turn and leaves it zeroed when it completes. Up to 64 such calls may
  *     run on one device at the same time (on different streams); more are not
  *     supported. Calls may be captured in a CUDA graph: a captured call keeps
