@@ -624,6 +624,44 @@ def main(argv=None):
                                "gbs": pack_bytes / (wms * 1e-3) / 1e9,
                                "pct_hbm": 100 * pack_bytes / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
+    # ---- bounded depth cache: slot utilities (depth mass) and the slot choice ----
+    if w.L:
+        mass = torch.empty((w.Hk, w.L), dtype=torch.float32, device=dev)
+        mws = torch.empty(((moda.moda_depth_mass_workspace_bytes(w.T, w.Hk, w.L) + 3) // 4,),
+                          dtype=torch.float32, device=dev)
+        slot_age = torch.arange(w.L, dtype=torch.int32, device=dev)  # a full cache, oldest in slot 0
+        slot = torch.empty((1,), dtype=torch.int32, device=dev)
+        moda.moda_fwd(q, k, v, kd, vd, w.scale, o=o, lse=lse, stream=stream)
+        for _ in range(2):
+            moda.moda_depth_mass(q, kd, lse, w.scale, mass=mass, workspace=mws, stream=stream)
+        em = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(5)]
+        torch.cuda.synchronize(dev)
+        for a, b in em:  # q and kd (3.5 GB at the long workload) are far larger than L2
+            a.record(stream)
+            moda.moda_depth_mass(q, kd, lse, w.scale, mass=mass, workspace=mws, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        mms = statistics.median(a.elapsed_time(b) for a, b in em)
+        mbytes = q.numel() * 2 + kd.numel() * 2 + lse.numel() * 4 + mass.numel() * 4
+        ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(5)]
+        for i, (a, b) in enumerate(ea):
+            a.record(stream)
+            moda.moda_depth_cache_admit(slot_age, mass, w.L // 2, w.L + i, slot=slot, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ams = statistics.median(a.elapsed_time(b) for a, b in ea)
+        line["depth_cache"] = {
+            "depth_mass_ms": mms, "depth_mass_bytes": mbytes,
+            "gbs": mbytes / (mms * 1e-3) / 1e9,
+            "pct_hbm": 100 * mbytes / (mms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "admit_us": 1e3 * ams, "slots": w.L, "recent": w.L // 2,
+            "note": "moda_depth_mass: each slot's probability mass in the joint softmax, summed "
+                    "over rows and KV heads (reads q, the packed kd and lse once); "
+                    "moda_depth_cache_admit: the hybrid slot choice on a full cache"}
+        del mass, mws, slot_age, slot
+
     # ---- decode: the last position as a new token over the whole cache ----
     if args.decode_steps > 0:
         t = w.T - 1

@@ -18,103 +18,209 @@
 #include <cuda_bf16.h>
 
 #include "moda_internal.h"
+#include "sm103.cuh"
+#include "warp_mma.cuh"
 
 namespace moda {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kChunk = 64;  // positions per CTA of the mass kernel
+constexpr int kMassWarps = 4;     // warps per CTA of the mass kernel
+constexpr int kMassMaxCtas = 2048;  // CTAs over all KV heads (per-CTA partials)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// CTAs per KV head of the mass kernel; each takes a contiguous run of
+// positions, its warps the run's positions in turn.
+int mass_blocks(int T, int Hk) {
+  const int per_head = kMassMaxCtas / Hk > 1 ? kMassMaxCtas / Hk : 1;
+  const int need = (T + kMassWarps - 1) / kMassWarps;
+  return need < per_head ? need : per_head;
+}
+
+// One warp's shared memory: two buffers of 32 staged depth-key rows (the
+// chunk being scored and the next one, in flight) and two of the G query
+// rows (this position's and the next one's; rows G..R-1 zero).
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32)
+struct alignas(16) MassWarpSmem {
+  static constexpr int R = G < 8 ? 8 : G;  // query rows held as A-tile rows
+  static constexpr int QS = D + 8;         // padded row: ldmatrix rows in distinct banks
+  uint4 kr[2][32][D / 8];
+  __nv_bfloat16 qs[2][R][QS];
+};
+
+// Each warp walks its positions' slots in chunks of 32 (work item k = the
+// position's chunk), staging item k+1 by 16-byte cp.async while it scores
+// item k on warp-level tensor-core MMAs (mma.sync m16n8k16; the G query rows
+// are rows 0..G-1 of the A tiles): S = Q Kd^T (16 x 32), then per slot the
+// sum over the G rows of exp2(S scale log2e - lse log2e), added to the warp's
+// running mass of that slot. The warps' sums are added in a fixed order into
+// one partial row per CTA, and depth_mass_reduce_kernel adds those in a fixed
+// order, so the result does not depend on scheduling.
+template <int D, int G>
+__global__ void __launch_bounds__(kMassWarps * 32)
 depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kd,
-                  const float* __restrict__ lse, int T, int Hq, int L, float scale_log2,
-                  float* __restrict__ partial) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  // [kWarps][G][D] query rows of the position a warp works on, then
-  // [kWarps][L] per-warp slot sums
-  __nv_bfloat16* qs_all = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  float* acc_all = reinterpret_cast<float*>(smem_raw + (size_t)kWarps * G * D * 2);
+                  const float* __restrict__ lse, int T, int Hq, int L, int run,
+                  float scale_log2, float* __restrict__ partial) {
+  using W = MassWarpSmem<D, G>;
+  using namespace wmma16;
+  constexpr int CH = D / 8;    // 16-byte pieces per row
+  constexpr bool kHi = G > 8;  // rows 8..15 of the A tiles hold query heads
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk = blockIdx.x, hk = blockIdx.y, nchunks = gridDim.x;
-  __nv_bfloat16* qs = qs_all + (size_t)warp * G * D;
+  W& sm = reinterpret_cast<W*>(smem_raw)[warp];
+  float* acc_all = reinterpret_cast<float*>(smem_raw + sizeof(W) * kMassWarps);
   float* acc = acc_all + (size_t)warp * L;
+  const int hk = blockIdx.y;
+  const int t0 = blockIdx.x * run, t1 = min(T, t0 + run);
+  const int npos = t1 - t0 > warp ? (t1 - t0 - warp + kMassWarps - 1) / kMassWarps : 0;
+  const int nch = (L + 31) / 32;
+  const int nitems = npos * nch;
   for (int l = lane; l < L; l += 32) acc[l] = 0.f;
-  for (int tt = warp; tt < kChunk; tt += kWarps) {
-    const int t = chunk * kChunk + tt;
-    if (t >= T) break;
-    const int64_t row0 = (int64_t)t * Hq + hk * G;
-    __syncwarp();
-    for (int idx = lane; idx < G * D / 8; idx += 32)
-      reinterpret_cast<uint4*>(qs)[idx] = __ldg(reinterpret_cast<const uint4*>(q + row0 * D) + idx);
-    float lg[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) lg[g] = __ldg(lse + row0 + g) * kLog2e;
-    __syncwarp();
-    const int64_t slot0 = ((int64_t)hk * T + t) * L;
-    for (int l = lane; l < L; l += 32) {
-      // lane owns slot l: its G logits from one read of the slot's key row
-      const uint4* kr = reinterpret_cast<const uint4*>(kd + (slot0 + l) * D);
-      float s[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] = 0.f;
+
+  // byte offset of 16-byte piece c of staged row r (XOR-swizzled by r)
+  auto piece = [](int r, int c) -> uint32_t { return (uint32_t)((r * CH + (c ^ (r & (CH - 1)))) * 16); };
+  const int g_lo = lane >> 2;
+  float lse0_lo = 0.f, lse0_hi = 0.f, lse1_lo = 0.f, lse1_hi = 0.f;  // by position parity
+  // stage item k: its 32 key rows (rows past L zero-filled) and, for a
+  // position's first chunk, the position's query rows and lse values
+  auto issue = [&](int k) {
+    const int i = k / nch, c = k - i * nch;
+    const int t = t0 + warp + i * kMassWarps;
+    const int l0 = c * 32, nl = min(32, L - l0);
+    const int64_t slot0 = ((int64_t)hk * T + t) * L + l0;
+    const uint32_t kr0 = sm103::smem_u32(&sm.kr[k & 1][0][0]);
 #pragma unroll 4
-      for (int ch = 0; ch < D / 8; ++ch) {
-        const uint4 kc = __ldg(kr + ch);
-        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kc);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const uint4 qc = reinterpret_cast<const uint4*>(qs + g * D)[ch];
-          const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 a = __bfloat1622float2(q2[i]), b = __bfloat1622float2(k2[i]);
-            s[g] = fmaf(a.x, b.x, fmaf(a.y, b.y, s[g]));
-          }
-        }
-      }
-      float m = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) m += exp2f(s[g] * scale_log2 - lg[g]);
-      acc[l] += m;
+    for (int idx = lane; idx < 32 * CH; idx += 32) {
+      const int r = idx / CH, cc = idx % CH;
+      const bool ok = r < nl;
+      cp_async16(kr0 + piece(r, cc), kd + (slot0 + (ok ? r : 0)) * D + cc * 8, ok ? 16u : 0u);
     }
+    if (c == 0) {
+      const int64_t row0 = (int64_t)t * Hq + hk * G;
+      for (int idx = lane; idx < W::R * CH; idx += 32) {
+        const int g = idx / CH, cc = idx % CH;
+        cp_async16(sm103::smem_u32(&sm.qs[i & 1][g][cc * 8]), q + (row0 + (g < G ? g : 0)) * D + cc * 8,
+                   g < G ? 16u : 0u);
+      }
+      const float lo = g_lo < G ? __ldg(lse + row0 + g_lo) * kLog2e : 0.f;
+      const float hi = kHi ? __ldg(lse + row0 + g_lo + 8) * kLog2e : 0.f;
+      if (i & 1) {
+        lse1_lo = lo;
+        lse1_hi = hi;
+      } else {
+        lse0_lo = lo;
+        lse0_hi = hi;
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+
+  const int lr = lane & 7, lm = lane >> 3;  // ldmatrix: the row this lane addresses, its matrix
+  if (nitems > 0) issue(0);
+  for (int k = 0; k < nitems; ++k) {
+    if (k + 1 < nitems) {
+      issue(k + 1);  // its buffers were last read by item k-1 (the __syncwarp below)
+      asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    }
+    __syncwarp();
+    const int i = k / nch, c = k - i * nch;
+    const int l0 = c * 32, nl = min(32, L - l0);
+    const float lse_lo = (i & 1) ? lse1_lo : lse0_lo, lse_hi = (i & 1) ? lse1_hi : lse0_hi;
+    const uint32_t kr0 = sm103::smem_u32(&sm.kr[k & 1][0][0]);
+    const uint32_t qs0 = sm103::smem_u32(&sm.qs[i & 1][0][0]);
+    // S = Q Kd^T: n-tile nt holds slots 8nt..8nt+7 of the chunk
+    float sc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t aq[4];
+      if constexpr (kHi) {
+        // matrices: rows 0-7 | rows 8-15, columns 16ks.. | 16ks+8..
+        ldsm_x4(qs0 + (uint32_t)(((lm & 1) * 8 + lr) * W::QS + ks * 16 + (lm >> 1) * 8) * 2, aq[0], aq[1],
+                aq[2], aq[3]);
+      } else {
+        ldsm_x2(qs0 + (uint32_t)(lr * W::QS + ks * 16 + (lm & 1) * 8) * 2, aq[0], aq[2]);
+        aq[1] = aq[3] = 0u;
+      }
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        // matrices: pieces 2ks, 2ks+1 of slots 16np..16np+7 | 16np+8..16np+15
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kr0 + piece(np * 16 + (lm >> 1) * 8 + lr, 2 * ks + (lm & 1)), b0, b1, b2, b3);
+        mma_bf16(sc[2 * np], aq, b0, b1);
+        mma_bf16(sc[2 * np + 1], aq, b2, b3);
+      }
+    }
+    // the slot's probability summed over this lane's rows (g_lo, g_lo + 8),
+    // then over the rows of the other lanes of the same column pair
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int sl = nt * 8 + 2 * (lane & 3);
+      const bool v0 = sl < nl, v1 = sl + 1 < nl;
+      float m0 = 0.f, m1 = 0.f;
+      if (g_lo < G) {
+        m0 = v0 ? exp2f(sc[nt][0] * scale_log2 - lse_lo) : 0.f;
+        m1 = v1 ? exp2f(sc[nt][1] * scale_log2 - lse_lo) : 0.f;
+      }
+      if constexpr (kHi) {
+        m0 += v0 ? exp2f(sc[nt][2] * scale_log2 - lse_hi) : 0.f;
+        m1 += v1 ? exp2f(sc[nt][3] * scale_log2 - lse_hi) : 0.f;
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        m0 += __shfl_xor_sync(0xffffffffu, m0, off);
+        m1 += __shfl_xor_sync(0xffffffffu, m1, off);
+      }
+      if (lane < 4) {
+        if (v0) acc[l0 + sl] += m0;
+        if (v1) acc[l0 + sl + 1] += m1;
+      }
+    }
+    __syncwarp();  // the staged rows of item k are read: item k+2 may take the buffers
   }
   __syncthreads();
   // this CTA's partial sums, warps added in a fixed order
-  float* out = partial + ((int64_t)hk * nchunks + chunk) * L;
-  for (int l = threadIdx.x; l < L; l += kWarps * 32) {
+  float* out = partial + ((int64_t)hk * gridDim.x + blockIdx.x) * L;
+  for (int l = threadIdx.x; l < L; l += kMassWarps * 32) {
     float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += acc_all[(size_t)w * L + l];
+    for (int w = 0; w < kMassWarps; ++w) s += acc_all[(size_t)w * L + l];
     out[l] = s;
   }
 }
 
-__global__ void depth_mass_reduce_kernel(const float* __restrict__ partial, int Hk, int nchunks,
-                                         int L, float* __restrict__ mass) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= Hk * L) return;
-  const int hk = i / L, l = i - hk * L;
-  const float* p = partial + (int64_t)hk * nchunks * L + l;
+// mass[hk][l] = the sum of the nblk partial rows of head hk: one warp per
+// output, lanes over the partials in a fixed order, then a fixed shuffle tree.
+__global__ void __launch_bounds__(256)
+depth_mass_reduce_kernel(const float* __restrict__ partial, int Hk, int nblk, int L,
+                         float* __restrict__ mass) {
+  const int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (w >= Hk * L) return;
+  const int hk = w / L, l = w - hk * L;
+  const float* p = partial + (int64_t)hk * nblk * L + l;
   float s = 0.f;
-  for (int c = 0; c < nchunks; ++c) s += p[(int64_t)c * L];
-  mass[i] = s;
+  for (int c = lane; c < nblk; c += 32) s += p[(int64_t)c * L];
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) mass[w] = s;
 }
 
 template <int D, int G>
 cudaError_t launch_mass_dg(const DepthMassArgs& a, cudaStream_t st) {
-  const int nchunks = (a.T + kChunk - 1) / kChunk;
-  const size_t smem = (size_t)kWarps * G * D * 2 + (size_t)kWarps * a.L * 4;
+  const int nblk = mass_blocks(a.T, a.Hk);
+  const int run = (a.T + nblk - 1) / nblk;
+  const size_t smem = sizeof(MassWarpSmem<D, G>) * kMassWarps + (size_t)kMassWarps * a.L * 4;
   cudaError_t e = cudaFuncSetAttribute(depth_mass_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  depth_mass_kernel<D, G><<<dim3(nchunks, a.Hk), kWarps * 32, smem, st>>>(
-      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, a.lse, a.T, a.Hq, a.L,
+  depth_mass_kernel<D, G><<<dim3(nblk, a.Hk), kMassWarps * 32, smem, st>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.kd, a.lse, a.T, a.Hq, a.L, run,
       a.scale * kLog2e, a.work);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int n = a.Hk * a.L;
-  depth_mass_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.work, a.Hk, nchunks, a.L, a.mass);
+  const int warps = a.Hk * a.L;
+  depth_mass_reduce_kernel<<<(warps + 7) / 8, 256, 0, st>>>(a.work, a.Hk, nblk, a.L, a.mass);
   return cudaGetLastError();
 }
 
@@ -206,7 +312,7 @@ __global__ void cache_admit_kernel(int* __restrict__ ages, const float* __restri
 }  // namespace
 
 size_t depth_mass_workspace_floats(int T, int Hk, int L) {
-  return (size_t)((T + kChunk - 1) / kChunk) * Hk * L;
+  return (size_t)mass_blocks(T, Hk) * Hk * L;
 }
 
 cudaError_t launch_depth_mass(const DepthMassArgs& a, cudaStream_t stream) {

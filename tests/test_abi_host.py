@@ -260,10 +260,12 @@ def test_decode_rejects(lib, kw, code):
 
 # ---- bounded depth cache entry points
 def test_depth_mass_workspace_formula(lib):
-    # one [L] partial per KV head and block of 64 positions
-    assert lib.moda_depth_mass_workspace_bytes(64, 4, 48) == 1 * 4 * 48 * 4
-    assert lib.moda_depth_mass_workspace_bytes(65536, 4, 48) == 1024 * 4 * 48 * 4
-    assert lib.moda_depth_mass_workspace_bytes(65, 2, 3) == 2 * 2 * 3 * 4
+    # one [L] partial per CTA: per KV head, ceil(T / 4) CTAs (four positions,
+    # one per warp, at least) up to 2048 CTAs over all heads
+    assert lib.moda_depth_mass_workspace_bytes(64, 4, 48) == 16 * 4 * 48 * 4
+    assert lib.moda_depth_mass_workspace_bytes(65536, 4, 48) == 512 * 4 * 48 * 4
+    assert lib.moda_depth_mass_workspace_bytes(65, 2, 3) == 17 * 2 * 3 * 4
+    assert lib.moda_depth_mass_workspace_bytes(65536, 4096, 1) == 1 * 4096 * 1 * 4
     assert lib.moda_depth_mass_workspace_bytes(0, 4, 48) == 0
 
 
