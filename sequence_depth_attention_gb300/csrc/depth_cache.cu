@@ -101,8 +101,11 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         cp_async16(sm103::smem_u32(&sm.qs[i & 1][g][cc * 8]), q + (row0 + (g < G ? g : 0)) * D + cc * 8,
                    g < G ? 16u : 0u);
       }
-      const float lo = g_lo < G ? __ldg(lse + row0 + g_lo) * kLog2e : 0.f;
-      const float hi = kHi ? __ldg(lse + row0 + g_lo + 8) * kLog2e : 0.f;
+      // G > 8: rows g_lo and g_lo + 8 of S; else S^T, columns (heads)
+      // 2(lane%4) and 2(lane%4) + 1
+      const int h0 = kHi ? g_lo : 2 * (lane & 3), h1 = kHi ? g_lo + 8 : h0 + 1;
+      const float lo = h0 < G ? __ldg(lse + row0 + h0) * kLog2e : 0.f;
+      const float hi = h1 < G ? __ldg(lse + row0 + h1) * kLog2e : 0.f;
       if (i & 1) {
         lse1_lo = lo;
         lse1_hi = hi;
@@ -129,54 +132,81 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const float lse_lo = (i & 1) ? lse1_lo : lse0_lo, lse_hi = (i & 1) ? lse1_hi : lse0_hi;
     const uint32_t kr0 = sm103::smem_u32(&sm.kr[k & 1][0][0]);
     const uint32_t qs0 = sm103::smem_u32(&sm.qs[i & 1][0][0]);
-    // S = Q Kd^T: n-tile nt holds slots 8nt..8nt+7 of the chunk
-    float sc[4][4];
+    if constexpr (kHi) {
+      // S = Q Kd^T: n-tile nt holds slots 8nt..8nt+7 of the chunk
+      float sc[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t aq[4];
-      if constexpr (kHi) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         // matrices: rows 0-7 | rows 8-15, columns 16ks.. | 16ks+8..
+        uint32_t aq[4];
         ldsm_x4(qs0 + (uint32_t)(((lm & 1) * 8 + lr) * W::QS + ks * 16 + (lm >> 1) * 8) * 2, aq[0], aq[1],
                 aq[2], aq[3]);
-      } else {
-        ldsm_x2(qs0 + (uint32_t)(lr * W::QS + ks * 16 + (lm & 1) * 8) * 2, aq[0], aq[2]);
-        aq[1] = aq[3] = 0u;
-      }
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        // matrices: pieces 2ks, 2ks+1 of slots 16np..16np+7 | 16np+8..16np+15
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kr0 + piece(np * 16 + (lm >> 1) * 8 + lr, 2 * ks + (lm & 1)), b0, b1, b2, b3);
-        mma_bf16(sc[2 * np], aq, b0, b1);
-        mma_bf16(sc[2 * np + 1], aq, b2, b3);
+        for (int np = 0; np < 2; ++np) {
+          // matrices: pieces 2ks, 2ks+1 of slots 16np..16np+7 | 16np+8..16np+15
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kr0 + piece(np * 16 + (lm >> 1) * 8 + lr, 2 * ks + (lm & 1)), b0, b1, b2, b3);
+          mma_bf16(sc[2 * np], aq, b0, b1);
+          mma_bf16(sc[2 * np + 1], aq, b2, b3);
+        }
       }
-    }
-    // the slot's probability summed over this lane's rows (g_lo, g_lo + 8),
-    // then over the rows of the other lanes of the same column pair
+      // the slot's probability summed over this lane's rows (g_lo, g_lo + 8),
+      // then over the rows of the other lanes of the same column pair
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int sl = nt * 8 + 2 * (lane & 3);
-      const bool v0 = sl < nl, v1 = sl + 1 < nl;
-      float m0 = 0.f, m1 = 0.f;
-      if (g_lo < G) {
-        m0 = v0 ? exp2f(sc[nt][0] * scale_log2 - lse_lo) : 0.f;
-        m1 = v1 ? exp2f(sc[nt][1] * scale_log2 - lse_lo) : 0.f;
-      }
-      if constexpr (kHi) {
+      for (int nt = 0; nt < 4; ++nt) {
+        const int sl = nt * 8 + 2 * (lane & 3);
+        const bool v0 = sl < nl, v1 = sl + 1 < nl;
+        float m0 = v0 ? exp2f(sc[nt][0] * scale_log2 - lse_lo) : 0.f;
+        float m1 = v1 ? exp2f(sc[nt][1] * scale_log2 - lse_lo) : 0.f;
         m0 += v0 ? exp2f(sc[nt][2] * scale_log2 - lse_hi) : 0.f;
         m1 += v1 ? exp2f(sc[nt][3] * scale_log2 - lse_hi) : 0.f;
-      }
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        m0 += __shfl_xor_sync(0xffffffffu, m0, off);
-        m1 += __shfl_xor_sync(0xffffffffu, m1, off);
+        for (int off = 4; off < 32; off <<= 1) {
+          m0 += __shfl_xor_sync(0xffffffffu, m0, off);
+          m1 += __shfl_xor_sync(0xffffffffu, m1, off);
+        }
+        if (lane < 4) {
+          if (v0) acc[l0 + sl] += m0;
+          if (v1) acc[l0 + sl + 1] += m1;
+        }
       }
-      if (lane < 4) {
-        if (v0) acc[l0 + sl] += m0;
-        if (v1) acc[l0 + sl + 1] += m1;
+    } else {
+      // G <= 8: S^T = Kd Q^T, the chunk's 32 slots as two 16-row A tiles and
+      // the G heads as the 8 columns of one B tile (heads >= G zero), half
+      // the MMAs of S = Q Kd^T with the G rows padded to 16
+      float st[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) st[mt][0] = st[mt][1] = st[mt][2] = st[mt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        // B: heads (rows of the staged q) x columns 16ks.. | 16ks+8..
+        uint32_t bq0, bq1;
+        ldsm_x2(qs0 + (uint32_t)(lr * W::QS + ks * 16 + (lm & 1) * 8) * 2, bq0, bq1);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          // A: slots 16mt..+7 | 16mt+8..+15, pieces 2ks | 2ks+1
+          uint32_t a[4];
+          ldsm_x4(kr0 + piece(mt * 16 + (lm & 1) * 8 + lr, 2 * ks + (lm >> 1)), a[0], a[1], a[2], a[3]);
+          mma_bf16(st[mt], a, bq0, bq1);
+        }
       }
+      // per slot (rows g_lo, g_lo + 8 of each tile) the probabilities of this
+      // lane's two heads, then the other heads of the row's lane quad
+      const bool e0 = 2 * (lane & 3) < G, e1 = 2 * (lane & 3) + 1 < G;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int sl = mt * 16 + hh * 8 + g_lo;
+          const bool v = sl < nl;
+          float m = (v && e0) ? exp2f(st[mt][2 * hh] * scale_log2 - lse_lo) : 0.f;
+          m += (v && e1) ? exp2f(st[mt][2 * hh + 1] * scale_log2 - lse_hi) : 0.f;
+          m += __shfl_xor_sync(0xffffffffu, m, 1);
+          m += __shfl_xor_sync(0xffffffffu, m, 2);
+          if ((lane & 3) == 0 && v) acc[l0 + sl] += m;
+        }
     }
     __syncwarp();  // the staged rows of item k are read: item k+2 may take the buffers
   }
