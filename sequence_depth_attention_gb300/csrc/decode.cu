@@ -10,8 +10,12 @@
 //           cache (the last CTA the depth slots) for the G heads of hk with
 //           an online softmax; TMA streams 64-key K and V boxes (128-byte
 //           swizzle) through a shared-memory ring while 4 warps score 16 keys
-//           each on mma.sync tensor cores (the G heads are the rows of the A
-//           operand, so the dot products need no cross-lane reduction).
+//           each on mma.sync tensor cores. For G <= 8 the products are
+//           transposed (S^T = K Q^T with the keys as the A rows and the G
+//           heads as one 8-column B tile, then O^T += V^T P^T), which takes
+//           half the MMAs of the G heads padded to 16 A rows; G = 16 fills
+//           those rows (S = Q K^T, O += P V). Neither needs a cross-lane
+//           reduction for the dot products.
 //           Each CTA writes a partial (m, l, unnormalised o) to the workspace.
 //   pass 2  grid Hq: merge the nsplit + 1 partials of each head, o = O / l.
 #include <cuda_bf16.h>
@@ -115,126 +119,239 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   // the combine kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // Q as the A operand (row r = query head hk*G + r, k = the head dimension)
-  const int r0 = lane >> 2, cq = (lane & 3) * 2;
-  uint32_t qa[D / 16][4];
-  {
-    auto ld = [&](int r, int c) -> uint32_t {
-      return r < G ? *reinterpret_cast<const uint32_t*>(q + (int64_t)(hk * G + r) * D + c) : 0u;
-    };
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      qa[ks][0] = ld(r0, ks * 16 + cq);
-      qa[ks][1] = ld(r0 + 8, ks * 16 + cq);
-      qa[ks][2] = ld(r0, ks * 16 + 8 + cq);
-      qa[ks][3] = ld(r0 + 8, ks * 16 + 8 + cq);
-    }
-  }
-  float o[D / 8][4];
-#pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY;  // rows r0 and r0 + 8, log2 units
-  float l0 = 0.f, l1 = 0.f;              // this lane's share of the row sums
-
-  // ldmatrix source rows of this lane: K (x4 = key halves x dimension halves
-  // of one k16 step), V (x4.trans = key halves x two 8-column groups)
-  const int kkey = warp * kKW + ((lane >> 4) << 3) + (lane & 7), kcol = ((lane >> 3) & 1) * 8;
-  const int vkey = warp * kKW + (((lane >> 3) & 1) << 3) + (lane & 7), vcol = (lane >> 4) * 8;
-
-  int issued = min(NS, nblk);
-  for (int b = 0; b < nblk; ++b) {
-    const int s = b % NS;
-    bool ok = sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[s]), (b / NS) & 1, &sm.abort,
-                                       kTimeoutNs);
-    if (!__syncthreads_and(ok)) break;
-    const int jw = j0 + b * kKB + warp * kKW;  // this warp's first key
-    if (jw < j1) {
-      const uint32_t kb = sm103::smem_u32(&sm.u.ring[s][0][0]);
-      const uint32_t vb = sm103::smem_u32(&sm.u.ring[s][1][0]);
-      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  if constexpr (G <= 8) {
+    // G <= 8: the transposed products, half the MMAs of the G rows padded to
+    // 16: S^T = K Q^T (the warp's 16 keys as the rows of the A tile, the G
+    // heads as the 8 columns of the B tile) and O^T += V^T P^T (the head
+    // dimension in 16-row A tiles of V read transposed, P^T as the B tile).
+    // This lane's heads are hq and hq + 1; its rows are key (or dimension)
+    // r0 and r0 + 8 of a tile.
+    const int r0 = lane >> 2, hq = (lane & 3) * 2;
+    uint32_t qb[D / 16][2];  // B = Q^T: k = the head dimension, n = the head
+    {
+      auto ld = [&](int h, int c) -> uint32_t {
+        return h < G ? *reinterpret_cast<const uint32_t*>(q + (int64_t)(hk * G + h) * D + c) : 0u;
+      };
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t b00, b01, b10, b11;
-        wmma16::ldsm_x4(kb + swz128(kkey, ks * 16 + kcol), b00, b01, b10, b11);
-        wmma16::mma_bf16(c[0], qa[ks], b00, b01);
-        wmma16::mma_bf16(c[1], qa[ks], b10, b11);
-      }
-      // scores in log2 units; keys at or past j1 do not exist
-      float sv[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sv[nt][e] = jw + nt * 8 + cq + (e & 1) < j1 ? c[nt][e] * scale_log2 : -INFINITY;
-      float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-      float mx1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
-      const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-      m0 = n0;
-      m1 = n1;
-      float p[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = exp2f(sv[nt][0] - ref0);
-        p[nt][1] = exp2f(sv[nt][1] - ref0);
-        p[nt][2] = exp2f(sv[nt][2] - ref1);
-        p[nt][3] = exp2f(sv[nt][3] - ref1);
-      }
-      l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-      l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-      uint32_t pa[4];
-      pa[0] = wmma16::pack_bf16(p[0][0], p[0][1]);
-      pa[1] = wmma16::pack_bf16(p[0][2], p[0][3]);
-      pa[2] = wmma16::pack_bf16(p[1][0], p[1][1]);
-      pa[3] = wmma16::pack_bf16(p[1][2], p[1][3]);
-#pragma unroll
-      for (int nd = 0; nd < D / 8; nd += 2) {
-        uint32_t v0, v1, v2, v3;
-        wmma16::ldsm_x4_t(vb + swz128(vkey, nd * 8 + vcol), v0, v1, v2, v3);
-        o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
-        o[nd + 1][0] *= a0; o[nd + 1][1] *= a0; o[nd + 1][2] *= a1; o[nd + 1][3] *= a1;
-        wmma16::mma_bf16(o[nd], pa, v0, v1);
-        wmma16::mma_bf16(o[nd + 1], pa, v2, v3);
+        qb[ks][0] = ld(r0, ks * 16 + hq);
+        qb[ks][1] = ld(r0, ks * 16 + 8 + hq);
       }
     }
-    __syncthreads();  // stage s is free
-    if (tid == 0 && issued < nblk) {
-      issue(issued);
-      ++issued;
-    }
-  }
-  // in-flight copies land before the ring is reused or the CTA exits
-  if (tid == 0) {
-    int never = 0;
-    for (int b = max(0, issued - NS); b < issued; ++b)
-      sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[b % NS]), (b / NS) & 1, &never, kTimeoutNs);
-    if (sm.abort) atomicCAS(err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  __syncthreads();
-  // merge the warps of the CTA through shared memory (the ring is idle now)
+    float o[D / 16][4];  // O^T: rows = dimension, columns = heads hq, hq + 1
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    sm.u.merge.o[warp][r0][nd * 8 + cq] = o[nd][0];
-    sm.u.merge.o[warp][r0][nd * 8 + cq + 1] = o[nd][1];
-    sm.u.merge.o[warp][r0 + 8][nd * 8 + cq] = o[nd][2];
-    sm.u.merge.o[warp][r0 + 8][nd * 8 + cq + 1] = o[nd][3];
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float ma = -INFINITY, mb = -INFINITY;  // heads hq, hq + 1, log2 units
+    float la = 0.f, lb = 0.f;              // this lane's share of their sums
+    const int lr = lane & 7, lm = lane >> 3;
+    // ldmatrix rows of this lane: K (x4: key halves x dimension halves of one
+    // k16 step), V (x4.trans: dimension halves x key halves of a 16-row tile)
+    const int kkey = warp * kKW + (lm & 1) * 8 + lr, kcol = (lm >> 1) * 8;
+    const int vkey = warp * kKW + (lm >> 1) * 8 + lr, vcol = (lm & 1) * 8;
+
+    int issued = min(NS, nblk);
+    for (int b = 0; b < nblk; ++b) {
+      const int s = b % NS;
+      bool ok = sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[s]), (b / NS) & 1, &sm.abort,
+                                         kTimeoutNs);
+      if (!__syncthreads_and(ok)) break;
+      const int jw = j0 + b * kKB + warp * kKW;  // this warp's first key
+      if (jw < j1) {
+        const uint32_t kb = sm103::smem_u32(&sm.u.ring[s][0][0]);
+        const uint32_t vb = sm103::smem_u32(&sm.u.ring[s][1][0]);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a[4];
+          wmma16::ldsm_x4(kb + swz128(kkey, ks * 16 + kcol), a[0], a[1], a[2], a[3]);
+          wmma16::mma_bf16(c, a, qb[ks][0], qb[ks][1]);
+        }
+        // scores in log2 units; keys at or past j1 do not exist
+        const bool k0 = jw + r0 < j1, k1 = jw + r0 + 8 < j1;
+        const float s0 = k0 ? c[0] * scale_log2 : -INFINITY, s1 = k0 ? c[1] * scale_log2 : -INFINITY;
+        const float s2 = k1 ? c[2] * scale_log2 : -INFINITY, s3 = k1 ? c[3] * scale_log2 : -INFINITY;
+        float xa = fmaxf(s0, s2), xb = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+          xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
+        }
+        const float na = fmaxf(ma, xa), nb = fmaxf(mb, xb);
+        const float refa = na == -INFINITY ? 0.f : na, refb = nb == -INFINITY ? 0.f : nb;
+        const float aa = exp2f(ma - refa), ab = exp2f(mb - refb);
+        ma = na;
+        mb = nb;
+        const float p0 = exp2f(s0 - refa), p1 = exp2f(s1 - refb);
+        const float p2 = exp2f(s2 - refa), p3 = exp2f(s3 - refb);
+        la = la * aa + (p0 + p2);
+        lb = lb * ab + (p1 + p3);
+        // P^T (rows = keys, columns = heads) transposed into the B tile
+        const uint32_t pb0 = wmma16::movmatrix_t(wmma16::pack_bf16(p0, p1));
+        const uint32_t pb1 = wmma16::movmatrix_t(wmma16::pack_bf16(p2, p3));
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a[4];
+          wmma16::ldsm_x4_t(vb + swz128(vkey, mt * 16 + vcol), a[0], a[1], a[2], a[3]);
+          o[mt][0] *= aa; o[mt][1] *= ab; o[mt][2] *= aa; o[mt][3] *= ab;
+          wmma16::mma_bf16(o[mt], a, pb0, pb1);
+        }
+      }
+      __syncthreads();  // stage s is free
+      if (tid == 0 && issued < nblk) {
+        issue(issued);
+        ++issued;
+      }
+    }
+    // in-flight copies land before the ring is reused or the CTA exits
+    if (tid == 0) {
+      int never = 0;
+      for (int b = max(0, issued - NS); b < issued; ++b)
+        sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[b % NS]), (b / NS) & 1, &never, kTimeoutNs);
+      if (sm.abort) atomicCAS(err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, off);
+      lb += __shfl_xor_sync(0xffffffffu, lb, off);
+    }
+    __syncthreads();
+    // merge the warps of the CTA through shared memory (the ring is idle now)
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      sm.u.merge.o[warp][hq][mt * 16 + r0] = o[mt][0];
+      sm.u.merge.o[warp][hq + 1][mt * 16 + r0] = o[mt][1];
+      sm.u.merge.o[warp][hq][mt * 16 + r0 + 8] = o[mt][2];
+      sm.u.merge.o[warp][hq + 1][mt * 16 + r0 + 8] = o[mt][3];
+    }
+    if (r0 == 0) {
+      sm.u.merge.ml[warp][hq][0] = ma;
+      sm.u.merge.ml[warp][hq][1] = la;
+      sm.u.merge.ml[warp][hq + 1][0] = mb;
+      sm.u.merge.ml[warp][hq + 1][1] = lb;
+    }
+    __syncthreads();
+  } else {
+    // Q as the A operand (row r = query head hk*G + r, k = the head dimension)
+    const int r0 = lane >> 2, cq = (lane & 3) * 2;
+    uint32_t qa[D / 16][4];
+    {
+      auto ld = [&](int r, int c) -> uint32_t {
+        return r < G ? *reinterpret_cast<const uint32_t*>(q + (int64_t)(hk * G + r) * D + c) : 0u;
+      };
+  #pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = ld(r0, ks * 16 + cq);
+        qa[ks][1] = ld(r0 + 8, ks * 16 + cq);
+        qa[ks][2] = ld(r0, ks * 16 + 8 + cq);
+        qa[ks][3] = ld(r0 + 8, ks * 16 + 8 + cq);
+      }
+    }
+    float o[D / 8][4];
+  #pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;  // rows r0 and r0 + 8, log2 units
+    float l0 = 0.f, l1 = 0.f;              // this lane's share of the row sums
+
+    // ldmatrix source rows of this lane: K (x4 = key halves x dimension halves
+    // of one k16 step), V (x4.trans = key halves x two 8-column groups)
+    const int kkey = warp * kKW + ((lane >> 4) << 3) + (lane & 7), kcol = ((lane >> 3) & 1) * 8;
+    const int vkey = warp * kKW + (((lane >> 3) & 1) << 3) + (lane & 7), vcol = (lane >> 4) * 8;
+
+    int issued = min(NS, nblk);
+    for (int b = 0; b < nblk; ++b) {
+      const int s = b % NS;
+      bool ok = sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[s]), (b / NS) & 1, &sm.abort,
+                                         kTimeoutNs);
+      if (!__syncthreads_and(ok)) break;
+      const int jw = j0 + b * kKB + warp * kKW;  // this warp's first key
+      if (jw < j1) {
+        const uint32_t kb = sm103::smem_u32(&sm.u.ring[s][0][0]);
+        const uint32_t vb = sm103::smem_u32(&sm.u.ring[s][1][0]);
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  #pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b00, b01, b10, b11;
+          wmma16::ldsm_x4(kb + swz128(kkey, ks * 16 + kcol), b00, b01, b10, b11);
+          wmma16::mma_bf16(c[0], qa[ks], b00, b01);
+          wmma16::mma_bf16(c[1], qa[ks], b10, b11);
+        }
+        // scores in log2 units; keys at or past j1 do not exist
+        float sv[2][4];
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sv[nt][e] = jw + nt * 8 + cq + (e & 1) < j1 ? c[nt][e] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+        float mx1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+        const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+        m0 = n0;
+        m1 = n1;
+        float p[2][4];
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          p[nt][0] = exp2f(sv[nt][0] - ref0);
+          p[nt][1] = exp2f(sv[nt][1] - ref0);
+          p[nt][2] = exp2f(sv[nt][2] - ref1);
+          p[nt][3] = exp2f(sv[nt][3] - ref1);
+        }
+        l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+        uint32_t pa[4];
+        pa[0] = wmma16::pack_bf16(p[0][0], p[0][1]);
+        pa[1] = wmma16::pack_bf16(p[0][2], p[0][3]);
+        pa[2] = wmma16::pack_bf16(p[1][0], p[1][1]);
+        pa[3] = wmma16::pack_bf16(p[1][2], p[1][3]);
+  #pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+          uint32_t v0, v1, v2, v3;
+          wmma16::ldsm_x4_t(vb + swz128(vkey, nd * 8 + vcol), v0, v1, v2, v3);
+          o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
+          o[nd + 1][0] *= a0; o[nd + 1][1] *= a0; o[nd + 1][2] *= a1; o[nd + 1][3] *= a1;
+          wmma16::mma_bf16(o[nd], pa, v0, v1);
+          wmma16::mma_bf16(o[nd + 1], pa, v2, v3);
+        }
+      }
+      __syncthreads();  // stage s is free
+      if (tid == 0 && issued < nblk) {
+        issue(issued);
+        ++issued;
+      }
+    }
+    // in-flight copies land before the ring is reused or the CTA exits
+    if (tid == 0) {
+      int never = 0;
+      for (int b = max(0, issued - NS); b < issued; ++b)
+        sm103::mbar_wait_bounded(sm103::smem_u32(&sm.full[b % NS]), (b / NS) & 1, &never, kTimeoutNs);
+      if (sm.abort) atomicCAS(err, 0u, (unsigned int)MODA_ERR_TIMEOUT);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();
+    // merge the warps of the CTA through shared memory (the ring is idle now)
+  #pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      sm.u.merge.o[warp][r0][nd * 8 + cq] = o[nd][0];
+      sm.u.merge.o[warp][r0][nd * 8 + cq + 1] = o[nd][1];
+      sm.u.merge.o[warp][r0 + 8][nd * 8 + cq] = o[nd][2];
+      sm.u.merge.o[warp][r0 + 8][nd * 8 + cq + 1] = o[nd][3];
+    }
+    if ((lane & 3) == 0) {
+      sm.u.merge.ml[warp][r0][0] = m0;
+      sm.u.merge.ml[warp][r0][1] = l0;
+      sm.u.merge.ml[warp][r0 + 8][0] = m1;
+      sm.u.merge.ml[warp][r0 + 8][1] = l1;
+    }
+    __syncthreads();
   }
-  if ((lane & 3) == 0) {
-    sm.u.merge.ml[warp][r0][0] = m0;
-    sm.u.merge.ml[warp][r0][1] = l0;
-    sm.u.merge.ml[warp][r0 + 8][0] = m1;
-    sm.u.merge.ml[warp][r0 + 8][1] = l1;
-  }
-  __syncthreads();
   for (int idx = tid; idx < G * D; idx += kW * 32) {
     const int g = idx / D, c = idx % D;
     float M = -INFINITY;
