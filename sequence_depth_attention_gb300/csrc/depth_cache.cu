@@ -41,7 +41,7 @@ int mass_blocks(int T, int Hk) {
 // rows (this position's and the next one's; rows G..R-1 zero).
 template <int D, int G>
 struct alignas(16) MassWarpSmem {
-  static constexpr int R = G < 8 ? 8 : G;  // query rows held as A-tile rows
+  static constexpr int R = G < 8 ? 8 : G;  // query rows held (rows of an 8- or 16-row MMA tile)
   static constexpr int QS = D + 8;         // padded row: ldmatrix rows in distinct banks
   uint4 kr[2][32][D / 8];
   __nv_bfloat16 qs[2][R][QS];
@@ -49,10 +49,12 @@ struct alignas(16) MassWarpSmem {
 
 // Each warp walks its positions' slots in chunks of 32 (work item k = the
 // position's chunk), staging item k+1 by 16-byte cp.async while it scores
-// item k on warp-level tensor-core MMAs (mma.sync m16n8k16; the G query rows
-// are rows 0..G-1 of the A tiles): S = Q Kd^T (16 x 32), then per slot the
-// sum over the G rows of exp2(S scale log2e - lse log2e), added to the warp's
-// running mass of that slot. The warps' sums are added in a fixed order into
+// item k on warp-level tensor-core MMAs (mma.sync m16n8k16): for G <= 8
+// S^T = Kd Q^T (the 32 slots as two 16-row A tiles, the G heads as the
+// columns of one 8-column B tile), for G = 16 S = Q Kd^T (the heads as the 16
+// rows of the A tile); then per slot the sum over the G heads of
+// exp2(S scale log2e - lse log2e), added to the warp's running mass of that
+// slot. The warps' sums are added in a fixed order into
 // one partial row per CTA, and depth_mass_reduce_kernel adds those in a fixed
 // order, so the result does not depend on scheduling.
 template <int D, int G>
