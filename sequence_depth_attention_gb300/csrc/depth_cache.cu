@@ -36,25 +36,28 @@ int mass_blocks(int T, int Hk) {
   return need < per_head ? need : per_head;
 }
 
-// One warp's shared memory: two buffers of 32 staged depth-key rows (the
+// One warp's shared memory: two buffers of CR staged depth-key rows (the
 // chunk being scored and the next one, in flight) and two of the G query
-// rows (this position's and the next one's; rows G..R-1 zero).
+// rows (this position's and the next one's; rows G..R-1 zero). Chunks of 16
+// slots (32 at G = 16) keep the shared memory of a warp small, so that four
+// CTAs, sixteen warps, stream their chunks on each SM.
 template <int D, int G>
 struct alignas(16) MassWarpSmem {
   static constexpr int R = G < 8 ? 8 : G;  // query rows held (rows of an 8- or 16-row MMA tile)
   static constexpr int QS = D + 8;         // padded row: ldmatrix rows in distinct banks
-  uint4 kr[2][32][D / 8];
+  static constexpr int CR = G == 16 ? 32 : 16;  // slots per chunk (CR)
+  uint4 kr[2][CR][D / 8];
   __nv_bfloat16 qs[2][R][QS];
 };
 
-// Each warp walks its positions' slots in chunks of 32 (work item k = the
+// Each warp walks its positions' slots in chunks of CR (work item k = the
 // position's chunk), staging item k+1 by 16-byte cp.async while it scores
 // item k on warp-level tensor-core MMAs (mma.sync m16n8k16): for G <= 8
-// S^T = Kd Q^T (the 32 slots as two 16-row A tiles, the G heads as the
+// S^T = Kd Q^T (the 16 slots as the rows of the A tile, the G heads as the
 // columns of one 8-column B tile), for G = 16 S = Q Kd^T (the heads as the 16
-// rows of the A tile); then per slot the sum over the G heads of
-// exp2(S scale log2e - lse log2e), added to the warp's running mass of that
-// slot. The warps' sums are added in a fixed order into
+// rows of the A tile, 32 slots as four 8-column B tiles); then per slot the
+// sum over the G heads of exp2(S scale log2e - lse log2e), added to the warp's
+// running mass of that slot. The warps' sums are added in a fixed order into
 // one partial row per CTA, and depth_mass_reduce_kernel adds those in a fixed
 // order, so the result does not depend on scheduling.
 template <int D, int G>
@@ -74,7 +77,7 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int hk = blockIdx.y;
   const int t0 = blockIdx.x * run, t1 = min(T, t0 + run);
   const int npos = t1 - t0 > warp ? (t1 - t0 - warp + kMassWarps - 1) / kMassWarps : 0;
-  const int nch = (L + 31) / 32;
+  const int nch = (L + W::CR - 1) / W::CR;
   const int nitems = npos * nch;
   for (int l = lane; l < L; l += 32) acc[l] = 0.f;
 
@@ -82,16 +85,16 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   auto piece = [](int r, int c) -> uint32_t { return (uint32_t)((r * CH + (c ^ (r & (CH - 1)))) * 16); };
   const int g_lo = lane >> 2;
   float lse0_lo = 0.f, lse0_hi = 0.f, lse1_lo = 0.f, lse1_hi = 0.f;  // by position parity
-  // stage item k: its 32 key rows (rows past L zero-filled) and, for a
+  // stage item k: its CR key rows (rows past L zero-filled) and, for a
   // position's first chunk, the position's query rows and lse values
   auto issue = [&](int k) {
     const int i = k / nch, c = k - i * nch;
     const int t = t0 + warp + i * kMassWarps;
-    const int l0 = c * 32, nl = min(32, L - l0);
+    const int l0 = c * W::CR, nl = min(W::CR, L - l0);
     const int64_t slot0 = ((int64_t)hk * T + t) * L + l0;
     const uint32_t kr0 = sm103::smem_u32(&sm.kr[k & 1][0][0]);
 #pragma unroll 4
-    for (int idx = lane; idx < 32 * CH; idx += 32) {
+    for (int idx = lane; idx < W::CR * CH; idx += 32) {
       const int r = idx / CH, cc = idx % CH;
       const bool ok = r < nl;
       cp_async16(kr0 + piece(r, cc), kd + (slot0 + (ok ? r : 0)) * D + cc * 8, ok ? 16u : 0u);
@@ -130,7 +133,7 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     }
     __syncwarp();
     const int i = k / nch, c = k - i * nch;
-    const int l0 = c * 32, nl = min(32, L - l0);
+    const int l0 = c * W::CR, nl = min(W::CR, L - l0);
     const float lse_lo = (i & 1) ? lse1_lo : lse0_lo, lse_hi = (i & 1) ? lse1_hi : lse0_hi;
     const uint32_t kr0 = sm103::smem_u32(&sm.kr[k & 1][0][0]);
     const uint32_t qs0 = sm103::smem_u32(&sm.qs[i & 1][0][0]);
@@ -175,19 +178,20 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
       }
     } else {
-      // G <= 8: S^T = Kd Q^T, the chunk's 32 slots as two 16-row A tiles and
+      // G <= 8: S^T = Kd Q^T, the chunk's slots as 16-row A tiles and
       // the G heads as the 8 columns of one B tile (heads >= G zero), half
       // the MMAs of S = Q Kd^T with the G rows padded to 16
-      float st[2][4];
+      constexpr int MT = W::CR / 16;  // 16-slot A tiles per chunk
+      float st[MT][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) st[mt][0] = st[mt][1] = st[mt][2] = st[mt][3] = 0.f;
+      for (int mt = 0; mt < MT; ++mt) st[mt][0] = st[mt][1] = st[mt][2] = st[mt][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         // B: heads (rows of the staged q) x columns 16ks.. | 16ks+8..
         uint32_t bq0, bq1;
         ldsm_x2(qs0 + (uint32_t)(lr * W::QS + ks * 16 + (lm & 1) * 8) * 2, bq0, bq1);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
           // A: slots 16mt..+7 | 16mt+8..+15, pieces 2ks | 2ks+1
           uint32_t a[4];
           ldsm_x4(kr0 + piece(mt * 16 + (lm & 1) * 8 + lr, 2 * ks + (lm >> 1)), a[0], a[1], a[2], a[3]);
@@ -198,7 +202,7 @@ depth_mass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       // lane's two heads, then the other heads of the row's lane quad
       const bool e0 = 2 * (lane & 3) < G, e1 = 2 * (lane & 3) + 1 < G;
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int sl = mt * 16 + hh * 8 + g_lo;
