@@ -8,7 +8,7 @@
 //
 // HBM-bound copy of 16-byte vectors: consecutive lanes walk the d/8 vectors
 // of one (t, hk) row, so reads are contiguous and each destination row of
-// d*2 bytes is written whole.
+// d*2 bytes is written whole; each thread keeps four loads in flight.
 #include "moda_internal.h"
 
 namespace moda {
@@ -31,14 +31,25 @@ depth_write_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int T
     }
   }
   const int vpr = 1 << lg_vpr;
-  for (int64_t n = (int64_t)blockIdx.x * kThreads + threadIdx.x; n < total_vec;
-       n += (int64_t)gridDim.x * kThreads) {
+  auto put = [&](int64_t n, const uint4& v) {
     const int c = (int)(n & (vpr - 1));
     const int64_t row = n >> lg_vpr;  // t*Hk + hk
     const int t = (int)(row / Hk);
     const int hk = (int)(row - (int64_t)t * Hk);
-    dst[(((int64_t)hk * T + t) * L + slot) * vpr + c] = __ldg(src + n);
+    dst[(((int64_t)hk * T + t) * L + slot) * vpr + c] = v;
+  };
+  // four loads in flight per thread before their stores, so that an SM keeps
+  // enough bytes in flight to cover the memory latency
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  int64_t n = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  for (; n + 3 * stride < total_vec; n += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __ldg(src + n + j * stride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) put(n + j * stride, v[j]);
   }
+  for (; n < total_vec; n += stride) put(n, __ldg(src + n));
 }
 
 }  // namespace
